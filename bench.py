@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark: paged MLA decode, nh128 b64 ctx8192 (bf16 cache, page_size 1).
+
+One step = one decode call (mla_decode_fwd + mla_decode_combine when the plan
+splits) over the whole batch, with every input already resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload dense|ragged_bf16|ragged_fp8|fp8_long|mtp]
+
+Prints ONE JSON line (rank 0).  ``value`` is the whole-job KV-cache read rate
+in TB/s (KV bytes of all ranks / max-over-ranks time); the per-call latency is
+in ``us_per_call``.  Under torchrun (N > 1) every rank runs an independent
+replica of the workload: the op has no exchange step, so there is no
+collective on the data path (scaling: weak).
+
+``--impl reference`` times the fp64 CPU oracle, as it stands, on a bounded
+sample of the same workload on this host's cores (there is no reference
+library to install: the pages hold no code).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import mla_synth as syn  # noqa: E402
+
+METRIC = "MLA decode µs/call & KV-cache TB/s (frac of roofline), nh128 b64 ctx8192"
+UNIT = "TB/s"
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+MI355X_HK_US = {"dense": 132.878}  # the pages' HK m16x8 time for this workload (other hardware)
+
+
+# ------------------------------------------------------------------ workload ---
+
+def make_workload(name: str, seed: int = 0) -> syn.Problem:
+    if name == "dense":
+        return syn.dense(64, 8192, seed=seed)
+    if name == "ragged_bf16":
+        return syn.ragged(syn.KV_BF16, seed=seed)
+    if name == "ragged_fp8":
+        return syn.ragged(syn.KV_FP8_E4M3, seed=seed)
+    if name == "fp8_long":
+        return syn.fp8_long(109440, seed=seed)
+    if name == "mtp":
+        return syn.mtp(64, 2, 1, seed=seed)
+    raise ValueError(name)
+
+
+def visible_keys(p: syn.Problem) -> np.ndarray:
+    """[B, Sq] keys each query token attends to."""
+    lens = p.seq_lens.astype(np.int64)[:, None]
+    i = np.arange(p.sq)[None, :]
+    n = lens - p.sq + i + 1 if p.causal else np.broadcast_to(lens, (p.batch, p.sq))
+    return np.clip(n, 0, lens)
+
+
+def algorithmic(p: syn.Problem):
+    """Bytes and FLOPs one decode call must move / do (no padding, no partials)."""
+    row_bytes = 1152 if p.kv_dtype == syn.KV_BF16 else 576
+    kv = int(p.seq_lens.astype(np.int64).sum()) * row_bytes
+    rows = p.batch * p.sq * p.heads
+    q_b = rows * 576 * 2
+    out_b = rows * 512 * 2 + rows * 4
+    bt_b = int(sum(-(-int(c) // p.page_size) for c in p.seq_lens)) * 4
+    flops = 2 * int(visible_keys(p).sum()) * p.heads * (576 + 512)
+    return dict(kv_bytes=kv, bytes=kv + q_b + out_b + bt_b + p.batch * 4, flops=flops)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- distributed ---
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max over ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job rate: every rank processed the same units; time is the max."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------- CPU oracle ---
+
+def oracle_sample_rate(p: syn.Problem, target_s: float = 12.0):
+    """Time the oracle on whole (sequence, all heads, all tokens) slices of the
+    workload, growing the sample until it takes ~target_s; returns (KV bytes
+    per second of the full workload extrapolated from the sample, description)."""
+    import oracle
+    oracle.build()
+    row_bytes = 1152 if p.kv_dtype == syn.KV_BF16 else 576
+    nb = 1
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode(p.q_bits, p.cache, p.kv_dtype, p.kv_scale, p.page_size, p.block_table,
+                      p.seq_lens, p.softmax_scale, p.causal, b_range=(0, nb))
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 3 or nb >= p.batch:
+            break
+        nb = min(p.batch, max(nb + 1, int(nb * target_s / max(dt, 1e-3) / 2)))
+    sample_keys = int(p.seq_lens[:nb].astype(np.int64).sum())
+    full_keys = int(p.seq_lens.astype(np.int64).sum())
+    t_full = dt * full_keys / max(sample_keys, 1)
+    kv_rate = full_keys * row_bytes / t_full
+    desc = (f"first {nb} of {p.batch} sequences (all {p.heads} heads x {p.sq} tokens, "
+            f"{sample_keys} keys) in {dt:.2f} s; full-batch time extrapolated by keys: "
+            f"{t_full:.1f} s")
+    return kv_rate, dt, nb, t_full, desc
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    p = make_workload(args.workload)
+    import oracle
+    oracle.build()
+    per_step = []
+    nb = None
+    for _ in range(args.warmup + args.steps):
+        rate, dt, nb, t_full, desc = oracle_sample_rate(p, target_s=max(2.0, 30.0 / max(1, args.steps + args.warmup)))
+        per_step.append((rate, t_full, desc))
+    timed = per_step[args.warmup:]
+    rate = statistics.median(r for r, _, _ in timed)
+    t_full = statistics.median(t for _, t, _ in timed)
+    value = rate / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_full * 1e3,
+        "us_per_call": t_full * 1e6, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": config_of(p, args.workload),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": timed[-1][2]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(p: syn.Problem, workload: str):
+    lens = p.seq_lens.astype(np.int64)
+    return {"workload": p.name, "workload_key": workload, "batch": p.batch, "heads": p.heads,
+            "sq": p.sq, "ctx": int(lens.max()) if len(set(lens.tolist())) == 1 else "ragged",
+            "sum_ctx": int(lens.sum()), "page_size": p.page_size,
+            "kv_dtype": "bf16" if p.kv_dtype == syn.KV_BF16 else "fp8_e4m3",
+            "causal": p.causal, "softmax_scale": p.softmax_scale,
+            "l2": "inputs larger than L2 (KV cache %.0f MB vs 129 MB L2), no flush"
+                  % (p.cache.nbytes / 1e6),
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------- GPU arm ---
+
+def run_gpu(args):
+    import torch
+    import paged_mla_decode_latent_gb300 as mla
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity import to_device
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mla.build()
+    p = make_workload(args.workload, seed=rank)
+    alg = algorithmic(p)
+    t = to_device(p, dev)
+    plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal)
+    ws = mla.workspace_for(plan, dev)
+    out = torch.empty((p.batch, p.sq, p.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.batch, p.sq, p.heads), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 1 + (1 if plan.num_splits > 1 else 0)
+
+    def step():
+        mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
+                out, lse, ws, stream)
+        mla.combine(plan, t["lens"], out, lse, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = mla.check(plan, ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} after warm-up")
+
+    # choose K so the timed region lasts long enough for clock samples
+    steps = args.steps
+    if steps <= 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / 5 / 1e3
+        steps = int(min(20000, max(20, math.ceil(2.5 / max(per, 1e-6)))))
+
+    n_ev = steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_f = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    clocks = ClockSampler(dev.index if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(steps):
+        ev_s[k].record(stream)
+        mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
+                out, lse, ws, stream)
+        ev_f[k].record(stream)
+        mla.combine(plan, t["lens"], out, lse, ws, stream)
+        ev_e[k].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop()
+    total_s = t_start.elapsed_time(t_end) / 1e3
+    fwd_ms = [ev_s[k].elapsed_time(ev_f[k]) for k in range(steps)]
+    step_ms = [ev_s[k].elapsed_time(ev_e[k]) for k in range(steps)]
+    st = mla.check(plan, ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} after the timed steps")
+
+    total_max = reduce_max(total_s, dev)
+    ms_per_step = total_max / steps * 1e3
+    fwd_mean_ms = statistics.mean(fwd_ms)
+    kv_rate = aggregate_rate(alg["kv_bytes"] * steps, world, total_max)
+
+    hbm, tc, tc_sus, peak_src = load_peaks()
+    t_hbm = alg["bytes"] / (hbm * 1e9)
+    t_tc = alg["flops"] / (tc * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved = alg["bytes"] / (fwd_mean_ms / 1e3) / 1e9
+        peak, unit = hbm, "GB/s"
+    else:
+        achieved = alg["flops"] / (fwd_mean_ms / 1e3) / 1e12
+        peak, unit = tc, "TFLOP/s"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+            "kernel": "mla_decode_fwd", "roofline_us": max(t_hbm, t_tc) * 1e6,
+            "alg_bytes_per_launch": alg["bytes"], "alg_flops_per_launch": alg["flops"],
+            "fwd_us_mean": fwd_mean_ms * 1e3, "fwd_us_median": statistics.median(fwd_ms) * 1e3}
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            tr = json.load(open(prof)).get(args.workload)
+            if tr and tr.get("kernel_rev") == kernel_revision():
+                roof["traffic"] = tr["dram_bytes_per_launch"]
+        except Exception:
+            pass
+
+    # end to end through the public API with host buffers: H2D of q, block
+    # table and lengths from pinned memory, decode, D2H of out and lse
+    e2e = e2e_measure(mla, p, t, plan, ws, stream, dev, max(10, min(steps, 400)), world)
+
+    line = {
+        "metric": METRIC, "value": kv_rate / 1e12, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if p.kv_dtype == syn.KV_BF16 else "fp8_e4m3->bf16",
+        "data": "synthetic (seeded N(0,1), numpy Philox)",
+        "config": dict(config_of(p, args.workload), splits=plan.num_splits,
+                       chunk_len=plan.chunk_len, num_sms=plan.num_sms),
+        "roofline": roof, "clocks": clk, "e2e": e2e,
+        "gpu_launches": steps * launches_per_step,
+        "context": {"mi355x_hk_m16x8_us": MI355X_HK_US.get(args.workload),
+                    "note": "the pages' MI355X time for this shape (fp8 kernels, other hardware)"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, dt, nb, t_full, desc = oracle_sample_rate(p)
+        import oracle
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(mla, p, t, plan, ws, stream, dev, steps, world):
+    import torch
+    q_h = t["q"].cpu().pin_memory()
+    bt_h = t["bt"].cpu().pin_memory()
+    lens_h = t["lens"].cpu().pin_memory()
+    out_h = torch.empty((p.batch, p.sq, p.heads, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((p.batch, p.sq, p.heads), dtype=torch.float32).pin_memory()
+    q_d, bt_d, lens_d = torch.empty_like(t["q"]), torch.empty_like(t["bt"]), torch.empty_like(t["lens"])
+    out_d = torch.empty((p.batch, p.sq, p.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse_d = torch.empty((p.batch, p.sq, p.heads), dtype=torch.float32, device=dev)
+
+    def one():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        mla.fwd(plan, q_d, t["cache"], t["scale"], bt_d, lens_d, p.softmax_scale, out_d, lse_d, ws,
+                stream)
+        mla.combine(plan, lens_d, out_d, lse_d, ws, stream)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = reduce_max(e0.elapsed_time(e1) / 1e3, dev)
+    kv = algorithmic(p)["kv_bytes"]
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + lens_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return {"value": aggregate_rate(kv * steps, world, sec) / 1e12, "unit": UNIT,
+            "us_per_call": sec / steps * 1e6, "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def kernel_revision() -> str:
+    """Hash of the kernel sources: traffic figures are void once it changes."""
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "paged_mla_decode_latent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="0 = enough for ~2.5 s of timed work")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dense",
+                    choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        if args.steps <= 0:
+            args.steps = 3
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,213 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) paged MLA decode library
+ * (libmla_decode.so).
+ *
+ * The operation: multi-head latent attention decode in the absorbed form over
+ * a paged latent KV cache.  For sequence b, query token i < Sq and head
+ * h < H, the 576-wide query row q[b,i,h,:] (512 latent + 64 rope dims) scores
+ * every visible 576-wide latent row of sequence b, gathered through the block
+ * table; a softmax over those scores weights the first 512 dims of the same
+ * rows:
+ *
+ *   n      = causal ? ctx_b - Sq + i + 1 : ctx_b        (clamped to [0, ctx_b])
+ *   row_j  = kv_scale * cache[block_table[b][j / page_size]][j % page_size][:]
+ *   z_j    = softmax_scale * <q[b,i,h,:], row_j>                  j < n
+ *   lse    = ln sum_j exp(z_j)                                     (natural log)
+ *   out[d] = sum_j exp(z_j - lse) * row_j[d]                       d < 512
+ *
+ * n == 0 gives out = 0 and lse = -inf.
+ *
+ * Where each part comes from:
+ *   - the 576-wide latent row whose first 512 dims are the value:
+ *     "[Perf][Kimi-K3] Cut MLA decode concat/cache epilogue latency"
+ *     (vLLM PR 54896), Purpose, item 1;
+ *   - the paged cache at a variable page size and the causal mask over the
+ *     1+MTP query tokens: "HK MLA: MI35x m16x8 retune, new m16x4 kernel,
+ *     page_size + mask support" (aiter PR 3072), Summary, track 1;
+ *   - the three-call interface (a sizes/plan step, a metadata step and the
+ *     launch, which must all agree on the partition): same page, Summary,
+ *     track 2 (get_mla_metadata_info_v1 / get_mla_metadata_v1_2_device and the
+ *     kernel launch "all agree");
+ *   - the split of each sequence's keys into chunks on the grid, with a grid
+ *     sized from the longest sequence and chunks past a sequence's end
+ *     returning at once: "perf(mla): chunk the non-FP4 gather_kv_b_proj over
+ *     KV" (aiter PR 4776), description, second and third paragraphs.  The
+ *     log-sum-exp merge of the chunk partials follows from the per-row LSE
+ *     output; the pages do not write it out.
+ *
+ * Conventions for every entry point:
+ *   - All pointers marked "device" are CUDA device pointers of the current
+ *     device; "host" pointers are ordinary host memory.  The caller owns every
+ *     buffer, the workspace included.  The library allocates nothing.
+ *   - Work is queued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream).  No entry point synchronises the host except
+ *     mla_decode_check, which says so.
+ *   - Errors are returned as mla_status codes (never thrown, never printed).
+ *     Arguments are validated on the host before anything is queued; when a
+ *     call returns an error nothing was queued.
+ *   - Conditions only the device can see (a block-table entry outside
+ *     [0, num_pages), a context longer than the plan covers, a wait that ran
+ *     past its iteration limit) never fault: the kernel clamps the access,
+ *     sets a bit in the status word inside the workspace and carries on or
+ *     stops early.  mla_decode_check reads that word.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,  /* a pointer, size or enum is out of range */
+  MLA_ERR_UNSUPPORTED = -2,  /* valid request this build does not implement */
+  MLA_ERR_WORKSPACE = -3,    /* workspace NULL, misaligned or too small */
+  MLA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+  MLA_ERR_DEVICE_CHECK = -5, /* device status word: bad page id or context */
+  MLA_ERR_TIMEOUT = -6       /* device status word: a bounded wait expired */
+} mla_status;
+
+/* Cache element types. */
+typedef enum mla_kv_dtype {
+  MLA_KV_BF16 = 0,     /* bfloat16 latent rows, 1152 bytes each */
+  MLA_KV_FP8_E4M3 = 1  /* OCP fp8 E4M3FN codes, 576 bytes each, times kv_scale */
+} mla_kv_dtype;
+
+/* Bits of the device status word (OR-ed together by the kernels). */
+#define MLA_DEVFLAG_BAD_PAGE 0x1   /* block-table entry outside [0, num_pages) */
+#define MLA_DEVFLAG_CTX_RANGE 0x2  /* seq_lens[b] beyond the plan's max_ctx  */
+#define MLA_DEVFLAG_TIMEOUT 0x4    /* a bounded barrier wait gave up         */
+#define MLA_DEVFLAG_Q_RANGE 0x8    /* fp8 path: |q| beyond the fp16 range    */
+
+#define MLA_DECODE_PLAN_VERSION 1
+#define MLA_D_QK 576 /* query/key row width: 512 latent + 64 rope */
+#define MLA_D_V 512  /* value width: the first 512 dims of the same row */
+
+/*
+ * The split-KV partition of one batch shape.  Plain old data: the caller owns
+ * it, may copy or serialise it, and passes it unchanged to the calls below.
+ * Fields are outputs of mla_decode_plan; callers do not edit them.
+ */
+typedef struct mla_decode_plan_t {
+  int32_t version;      /* MLA_DECODE_PLAN_VERSION */
+  int32_t batch;        /* B */
+  int32_t num_heads;    /* H */
+  int32_t sq;           /* query tokens per sequence, 1 + MTP */
+  int32_t page_size;    /* keys per cache page */
+  int32_t kv_dtype;     /* mla_kv_dtype */
+  int32_t causal;       /* 0 or 1 */
+  int32_t rows;         /* H * Sq: score rows per sequence */
+  int32_t row_tile;     /* rows one CTA pair handles (128) */
+  int32_t row_blocks;   /* ceil(rows / row_tile) */
+  int32_t max_ctx;      /* longest context the plan covers */
+  int32_t key_tile;     /* keys per pipeline stage (64) */
+  int32_t chunk_len;    /* keys per split, a multiple of key_tile */
+  int32_t num_splits;   /* splits per sequence = ceil(max_ctx / chunk_len) */
+  int32_t num_sms;      /* SM count the partition was balanced for */
+  int32_t cluster_size; /* CTAs cooperating on one (b, row block, split) */
+  int32_t grid_x, grid_y, grid_z; /* launch grid of mla_decode_fwd */
+  int32_t reserved0;
+  int64_t ws_partial_o_offset;   /* byte offset of fp32 [B, S, rows, 512] partials */
+  int64_t ws_partial_lse_offset; /* byte offset of fp32 [B, S, rows] partial LSEs */
+  int64_t ws_status_offset;      /* byte offset of the int32 device status word */
+  int64_t workspace_bytes;       /* bytes the caller must provide */
+} mla_decode_plan_t;
+
+/*
+ * mla_decode_plan -- choose the split-KV partition (the "metadata" step).
+ *
+ * seq_lens_host  host int32[batch]: keys per sequence, the Sq new tokens
+ *                included (the cache insert precedes the decode).  0 allowed.
+ * batch          1 .. 65535
+ * num_heads      1 .. 128 with num_heads * sq <= 1024
+ * sq             1 .. 16 query tokens per sequence
+ * page_size      1 .. 4096 keys per page
+ * kv_dtype       mla_kv_dtype
+ * causal         0: every token sees all keys; 1: token i sees ctx - Sq + i + 1
+ * num_sms        SMs to balance for; 0 queries the current device
+ * plan           host out-parameter
+ *
+ * The chunk length is a multiple of the 64-key tile, chosen by simulating
+ * the in-order block dispatch over the SMs for each candidate split count
+ * and keeping the fastest (partial-output traffic counted).  The plan stays
+ * valid for later calls whose contexts are all <= plan->max_ctx; splits past
+ * a shorter sequence's end exit at once.  Pure host code: queues nothing.
+ * Returns MLA_OK or MLA_ERR_INVALID_ARG / MLA_ERR_CUDA (num_sms query).
+ */
+int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int32_t num_heads,
+                    int32_t sq, int32_t page_size, int32_t kv_dtype, int32_t causal,
+                    int32_t num_sms, mla_decode_plan_t* plan);
+
+/*
+ * mla_decode_fwd -- the decode kernel: block-table gather, QK^T, masked
+ * online softmax and PV for every (sequence, row block, split).
+ *
+ * plan            host, from mla_decode_plan
+ * q               device bf16 [B, Sq, H, 576], contiguous, 16-byte aligned
+ * kv_cache        device [num_pages, page_size, 576] bf16 or e4m3 codes,
+ *                 contiguous, 16-byte aligned
+ * num_pages       pages in kv_cache (block-table entries are checked against it)
+ * kv_scale        device fp32[1]: dequant multiplier of the fp8 cache; NULL
+ *                 means 1.0; ignored for bf16
+ * block_table     device int32 [B, bt_stride]; entries past ceil(ctx_b /
+ *                 page_size) are never read
+ * bt_stride       int32 elements between consecutive sequences' tables
+ * seq_lens        device int32[B]; each <= plan->max_ctx and <= bt_stride *
+ *                 page_size
+ * softmax_scale   multiplier of the raw dot product (e.g. 1/sqrt(192))
+ * out             device bf16 [B, Sq, H, 512]
+ * lse             device fp32 [B, Sq, H] (natural-log LSE of the scaled scores)
+ * workspace       device, 256-byte aligned, >= plan->workspace_bytes; holds
+ *                 the split partials and the status word; reused across calls
+ * stream          cudaStream_t as void*
+ *
+ * With plan->num_splits == 1 this call writes out and lse itself.  Otherwise
+ * it writes per-split partials into the workspace and mla_decode_combine must
+ * follow on the same stream before out/lse are read.  Resets the status word
+ * (an async memset on `stream`) before the kernel.
+ */
+int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
+                   int64_t num_pages, const float* kv_scale, const int32_t* block_table,
+                   int64_t bt_stride, const int32_t* seq_lens, float softmax_scale,
+                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * mla_decode_combine -- log-sum-exp merge of the split partials:
+ *   L = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - L) * o_s,  lse = L
+ * over the splits of each row; splits with no keys (lse_s = -inf) carry no
+ * weight, and a row with no keys at all gets out = 0, lse = -inf.
+ *
+ * Arguments as in mla_decode_fwd (same plan, seq_lens, workspace, out, lse,
+ * stream).  A no-op returning MLA_OK when plan->num_splits == 1.
+ */
+int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens,
+                       void* workspace, size_t workspace_bytes, void* out, float* lse,
+                       void* stream);
+
+/*
+ * mla_decode_check -- synchronously read the device status word of the last
+ * call that used `workspace` on `stream`.  Blocks the host until `stream`
+ * drains.  *host_status receives the MLA_DEVFLAG_* bits (0 = clean).
+ * Returns MLA_OK, MLA_ERR_DEVICE_CHECK (a bad page id or context),
+ * MLA_ERR_TIMEOUT (a wait gave up) or MLA_ERR_CUDA.
+ */
+int mla_decode_check(const mla_decode_plan_t* plan, const void* workspace, void* stream,
+                     int32_t* host_status);
+
+/* Static text for a status code. */
+const char* mla_status_string(int status);
+
+/* Library version string, e.g. "mla_decode 0.1 sm_103a". */
+const char* mla_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,128 @@
+// api.cu -- host side of the C ABI: argument validation, workspace carving and
+// the launches of the fwd and combine kernels.  Nothing here allocates or
+// synchronises (mla_decode_check excepted, by contract).
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mla_decode.h"
+#include "internal.h"
+
+int mla_launch_fwd_simt(const mla::FwdParams& p, void* stream);
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_plan(const mla_decode_plan_t* plan) {
+  if (plan == nullptr || plan->version != MLA_DECODE_PLAN_VERSION) return MLA_ERR_INVALID_ARG;
+  if (plan->batch < 1 || plan->rows < 1 || plan->rows != plan->num_heads * plan->sq)
+    return MLA_ERR_INVALID_ARG;
+  if (plan->num_splits < 1 || plan->chunk_len < 1 || plan->num_splits > mla::kMaxSplits)
+    return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype != MLA_KV_BF16 && plan->kv_dtype != MLA_KV_FP8_E4M3)
+    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+int check_workspace(const mla_decode_plan_t* plan, const void* ws, size_t bytes) {
+  if (ws == nullptr || !aligned(ws, 256)) return MLA_ERR_WORKSPACE;
+  if ((int64_t)bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
+                              int64_t num_pages, const float* kv_scale,
+                              const int32_t* block_table, int64_t bt_stride,
+                              const int32_t* seq_lens, float softmax_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != MLA_OK) return st;
+  if (!q || !kv_cache || !block_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || bt_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (bt_stride * (int64_t)plan->page_size < (int64_t)plan->max_ctx) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;  // NaN
+
+  char* ws = static_cast<char*>(workspace);
+  mla::FwdParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.cache = kv_cache;
+  p.num_pages = num_pages;
+  p.kv_scale = plan->kv_dtype == MLA_KV_FP8_E4M3 ? kv_scale : nullptr;
+  p.bt = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.softmax_scale = softmax_scale;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.part_o = plan->num_splits > 1 ? reinterpret_cast<float*>(ws + plan->ws_partial_o_offset) : nullptr;
+  p.part_lse =
+      plan->num_splits > 1 ? reinterpret_cast<float*>(ws + plan->ws_partial_lse_offset) : nullptr;
+  p.status = reinterpret_cast<int32_t*>(ws + plan->ws_status_offset);
+  p.batch = plan->batch;
+  p.heads = plan->num_heads;
+  p.sq = plan->sq;
+  p.rows = plan->rows;
+  p.page_size = plan->page_size;
+  p.kv_dtype = plan->kv_dtype;
+  p.causal = plan->causal;
+  p.chunk_len = plan->chunk_len;
+  p.num_splits = plan->num_splits;
+  p.max_ctx = plan->max_ctx;
+  p.row_blocks = plan->row_blocks;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla_launch_fwd(p, stream) != 0) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+extern "C" int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens,
+                                  void* workspace, size_t workspace_bytes, void* out, float* lse,
+                                  void* stream) {
+  int st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != MLA_OK) return st;
+  if (!out || !lse || !seq_lens || !aligned(out, 16) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+  if (plan->num_splits == 1) return MLA_OK;
+  char* ws = static_cast<char*>(workspace);
+  mla::CombineParams c;
+  c.part_o = reinterpret_cast<const float*>(ws + plan->ws_partial_o_offset);
+  c.part_lse = reinterpret_cast<const float*>(ws + plan->ws_partial_lse_offset);
+  c.out = static_cast<uint16_t*>(out);
+  c.lse = lse;
+  c.batch = plan->batch;
+  c.rows = plan->rows;
+  c.num_splits = plan->num_splits;
+  if (mla_launch_combine(c, stream) != 0) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+extern "C" int mla_decode_check(const mla_decode_plan_t* plan, const void* workspace,
+                                void* stream, int32_t* host_status) {
+  int st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  if (workspace == nullptr || host_status == nullptr) return MLA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  const char* ws = static_cast<const char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, ws + plan->ws_status_offset, sizeof v, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  *host_status = v;
+  if (v & MLA_DEVFLAG_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (v != 0) return MLA_ERR_DEVICE_CHECK;
+  return MLA_OK;
+}
+
+int mla_launch_fwd(const mla::FwdParams& p, void* stream) { return mla_launch_fwd_simt(p, stream); }

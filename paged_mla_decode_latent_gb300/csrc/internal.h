@@ -1,0 +1,49 @@
+// internal.h -- constants and launch parameters shared by the library's
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kDQK = 576;       // query/key row: 512 latent + 64 rope
+constexpr int kDV = 512;        // value: first 512 dims of the same row
+constexpr int kRowTile = 128;   // score rows per CTA pair (the MMA M)
+constexpr int kKeyTile = 64;    // keys per pipeline stage (the QK^T MMA N)
+constexpr int kClusterSize = 2; // CTAs per work unit: each owns half the value dims
+constexpr int kMaxRows = 1024;  // H * Sq limit
+constexpr int kMaxSplits = 256; // split-count cap of the planner
+
+// Everything a fwd kernel needs, resolved on the host from the plan and the
+// caller's pointers.
+struct FwdParams {
+  const uint16_t* q;        // bf16 [B, Sq, H, 576]
+  const void* cache;        // [num_pages, ps, 576] bf16 or e4m3
+  int64_t num_pages;
+  const float* kv_scale;    // device fp32[1] or nullptr
+  const int32_t* bt;        // [B, bt_stride]
+  int64_t bt_stride;
+  const int32_t* seq_lens;  // [B]
+  float softmax_scale;
+  uint16_t* out;            // bf16 [B, Sq, H, 512]
+  float* lse;               // [B, Sq, H]
+  float* part_o;            // fp32 [B, S, rows, 512] (S > 1)
+  float* part_lse;          // fp32 [B, S, rows]      (S > 1)
+  int32_t* status;          // device status word
+  int batch, heads, sq, rows, page_size, kv_dtype, causal;
+  int chunk_len, num_splits, max_ctx, row_blocks;
+};
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* out;
+  float* lse;
+  int batch, rows, num_splits;
+};
+
+}  // namespace mla
+
+// Launchers (return a cudaError_t as int).
+int mla_launch_fwd(const mla::FwdParams& p, void* stream);
+int mla_launch_combine(const mla::CombineParams& p, void* stream);

@@ -1,0 +1,79 @@
+"""Shared helpers of the GPU parity tests: move a ``mla_synth.Problem`` to the
+device, run the library through its C ABI, and compare with the fp64 oracle.
+
+Tolerances (bf16 output against the fp64 oracle on the same bits):
+  max |out - ref|                 <= 1.5e-2
+  ||out - ref||_F / ||ref||_F     <= 4e-3
+  max |lse - ref_lse|             <= 1e-3
+Rows with no visible key must give out == 0 and lse == -inf exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import mla_synth as syn
+
+MAX_ABS = 1.5e-2
+REL_FRO = 4e-3
+LSE_ABS = 1e-3
+
+
+def to_device(p: syn.Problem, device="cuda"):
+    import torch
+    t = {}
+    t["q"] = torch.from_numpy(p.q_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    if p.kv_dtype == syn.KV_BF16:
+        t["cache"] = torch.from_numpy(p.cache.view(np.int16)).view(torch.bfloat16).to(device)
+    else:
+        t["cache"] = torch.from_numpy(p.cache).to(device)
+    t["bt"] = torch.from_numpy(p.block_table).to(device)
+    t["lens"] = torch.from_numpy(p.seq_lens).to(device)
+    t["scale"] = torch.tensor([p.kv_scale], dtype=torch.float32, device=device)
+    return t
+
+
+def run_gpu(p: syn.Problem, t=None, num_sms: int = 0, plan=None, workspace=None, check=True):
+    """Plan + fwd + combine through the C ABI; returns (out f64, lse f64, plan, status)."""
+    import torch
+    import paged_mla_decode_latent_gb300 as mla
+    if t is None:
+        t = to_device(p)
+    if plan is None:
+        plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal, num_sms)
+    ws = workspace if workspace is not None else mla.workspace_for(plan)
+    out = torch.full((p.batch, p.sq, p.heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.batch, p.sq, p.heads), float("nan"), dtype=torch.float32, device="cuda")
+    mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale, out, lse, ws)
+    mla.combine(plan, t["lens"], out, lse, ws)
+    status = mla.check(plan, ws) if check else 0
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy(), plan, status
+
+
+def oracle_full(p: syn.Problem, b_range=None):
+    import oracle
+    return oracle.decode(p.q_bits, p.cache, p.kv_dtype, p.kv_scale, p.page_size, p.block_table,
+                         p.seq_lens, p.softmax_scale, p.causal, b_range=b_range)
+
+
+def assert_close(out, lse, ref_out, ref_lse, what=""):
+    """The bar of the parity tests (see the module docstring)."""
+    out = np.asarray(out, np.float64)
+    ref_out = np.asarray(ref_out, np.float64)
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: -inf LSE pattern differs"
+    assert np.all(out[empty] == 0), f"{what}: rows with no keys must be zero"
+    ok = ~empty
+    if not ok.any():
+        return {}
+    o, r = out[ok], ref_out[ok]
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    err = np.abs(o - r)
+    max_abs = float(err.max())
+    fro = float(np.linalg.norm(o - r) / max(np.linalg.norm(r), 1e-30))
+    lse_err = float(np.abs(lse[ok] - ref_lse[ok]).max())
+    stats = dict(max_abs=max_abs, rel_fro=fro, lse_abs=lse_err)
+    assert max_abs <= MAX_ABS, f"{what}: max abs {max_abs:.3e} > {MAX_ABS} {stats}"
+    assert fro <= REL_FRO, f"{what}: rel Frobenius {fro:.3e} > {REL_FRO} {stats}"
+    assert lse_err <= LSE_ABS, f"{what}: lse abs {lse_err:.3e} > {LSE_ABS} {stats}"
+    return stats
