@@ -10,6 +10,7 @@
 #include "internal.h"
 
 int mla_launch_fwd_simt(const mla::FwdParams& p, void* stream);
+int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream);
 
 namespace {
 
@@ -48,6 +49,7 @@ extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, cons
       !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return MLA_ERR_INVALID_ARG;
   if (num_pages < 1 || bt_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (num_pages * (int64_t)plan->page_size >= ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
   if (bt_stride * (int64_t)plan->page_size < (int64_t)plan->max_ctx) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;  // NaN
 
@@ -125,4 +127,6 @@ extern "C" int mla_decode_check(const mla_decode_plan_t* plan, const void* works
   return MLA_OK;
 }
 
-int mla_launch_fwd(const mla::FwdParams& p, void* stream) { return mla_launch_fwd_simt(p, stream); }
+int mla_launch_fwd(const mla::FwdParams& p, void* stream) {
+  return mla_launch_fwd_sm103(p, stream);
+}

@@ -1,0 +1,658 @@
+// fwd_sm103.cu -- the decode kernel on the 5th-generation tensor cores.
+//
+// Work unit: one (sequence b, 128-row block, KV split) handled by a cluster of
+// two CTAs.  Rows are the Sq*H query rows of the sequence (token-major, as q
+// is laid out), padded to the MMA M of 128.  The fp32 output accumulator of
+// 128 rows x 512 value dims would fill all 512 TMEM columns of one SM, so the
+// two CTAs split the value dims: CTA r owns value dims [256r, 256r+256) and,
+// for the score contraction, the same 256 latent dims (CTA 0 also takes the
+// 64 rope dims).  Each CTA therefore reads only its part of every latent row.
+//
+// Per 64-key tile, in each CTA:
+//   loader warp   : block-table lookup, one TMA box (64 dims x 1 row) per key
+//                   and per 64-dim atom into a 128B-swizzled K-major stage.
+//   MMA warp      : S_part = Q_part K_part^T  (tcgen05, A = Q from TMEM,
+//                   CTA 0's rope part A from shared memory), then
+//                   O_half += P V_half        (A = P from TMEM, B = the same
+//                   stage read MN-major as V).
+//   softmax warps : read S_part from TMEM, swap it with the partner CTA over
+//                   distributed shared memory, add (identical order in both
+//                   CTAs, so both see bit-identical scores), mask, online
+//                   softmax with a lazily rescaled running max, P -> TMEM as
+//                   bf16 over the consumed score columns.
+// The epilogue normalises O and writes bf16 output (one split) or fp32
+// partials plus the per-row log-sum-exp (several splits).
+//
+// Sources: the 576-wide latent row whose first 512 dims are the value
+// ("[Perf][Kimi-K3] Cut MLA decode concat/cache epilogue latency", Purpose
+// item 1); paged cache at any page size and the causal MTP mask ("HK MLA:
+// MI35x m16x8 retune, new m16x4 kernel, page_size + mask support", Summary
+// track 1; its MI35x retune interleaves the output rescale with the PV GEMM
+// and uses 64-key blocks, which this kernel keeps); one program per (batch,
+// head group, KV chunk) with chunks past a sequence's end returning at once
+// ("perf(mla): chunk the non-FP4 gather_kv_b_proj over KV", description).
+//
+// Every wait is bounded (about 2 s of wall time).  A wait that runs out sets
+// MLA_DEVFLAG_TIMEOUT in the status word and the CTA winds down instead of
+// hanging the GPU.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mla_decode.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int T = mla::kKeyTile;       // 64 keys per tile
+constexpr int ATOM = T * 128;          // one 64-dim slab of a 16-bit stage: 64 keys x 128 B
+constexpr int ATOM8 = T * 64;          // the same slab of raw fp8 codes: 64 keys x 64 B
+constexpr int SLOTS = 5;               // slabs per stage (CTA 0: 4 value + 1 rope)
+constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
+constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
+constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
+constexpr int RECV = 128 * T * 4;      // one partner score tile, fp32
+constexpr int kThreads = 256;
+constexpr int kDequantWarp0 = 2;       // fp8 cache: warps 2-3 turn codes into f16
+constexpr int kSoftmaxWarp0 = 4;
+
+// Shared-memory plan.  bf16 cache: 3 operand stages filled by TMA.  fp8
+// cache: 3 raw stages filled by TMA + 2 f16 operand stages filled by the
+// dequant warps.
+template <bool kFp8>
+struct Layout {
+  static constexpr int NS = kFp8 ? 2 : 3;   // operand stages (what the MMA reads)
+  static constexpr int NR = kFp8 ? 3 : 0;   // raw fp8 stages
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
+  static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
+  static constexpr int OFF_RECV = OFF_QROPE + QROPE;
+  static constexpr int OFF_BAR = OFF_RECV + 2 * RECV;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+};
+static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
+static_assert(Layout<true>::SMEM_BYTES <= 232448, "fp8 smem");
+
+// TMEM columns
+constexpr uint32_t TM_O = 0;     // 256 fp32 columns: this CTA's value half
+constexpr uint32_t TM_Q = 256;   // 128 columns: 256 bf16 of Q, packed in pairs
+constexpr uint32_t TM_S = 384;   // two 64-column score buffers; P overwrites cols 0..31
+constexpr uint32_t TM_COLS = 512;
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before a rescale
+constexpr float kMaxSentinel = -1.0e30f;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct Bars {
+  uint64_t kv_full[3];    // operand stage ready (TMA bytes landed / dequant done)
+  uint64_t kv_empty[3];   // operand stage consumed by the MMAs
+  uint64_t raw_full[3];   // fp8: raw stage landed
+  uint64_t raw_empty[3];  // fp8: raw stage converted
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t recv_full[2];
+  uint64_t o_done;
+  uint64_t q_ready;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct Ctx {
+  int32_t* status;
+  volatile int32_t* abort;
+};
+
+// Wait used only while winding down after an abort: ignores the abort word,
+// gives up after 0.5 s.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kTimeoutNs / 4) return false;
+  }
+  return true;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and flags the status
+// word and the CTA's abort word) if the phase did not complete in time or
+// another warp of this CTA already gave up.
+template <bool kCluster>
+__device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity) {
+  if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+    return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+      return true;
+    if ((++n & 63) == 0) {
+      if (*c.abort) return false;
+      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
+        atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
+        *c.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// The same, decided for the whole warp: true only if every lane's wait
+// succeeded, so warp-collective tcgen05 instructions stay convergent.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_all(const Ctx& c, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait<kCluster>(c, bar, parity));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 codes (low byte = first) -> two f16 (exact: every e4m3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Eight bf16 -> eight f16 (exact for |x| in [2^-14, 65504]; flags larger values).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, bool& out_of_range) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    out_of_range |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+    w[i] = pack_f16(lo, hi);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// K-major, 128B-swizzled operand: rows 128 B apart, 8-row groups 1 KB apart.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) {
+  return ptx::smem_desc(addr, 16, 1024, 2);
+}
+
+// The same stage read MN-major as V (N = 256 value dims over 4 slabs 8 KB
+// apart, K = keys in 8-row groups 1 KB apart).
+__device__ __forceinline__ uint64_t vmajor_desc(uint32_t addr) {
+  return ptx::smem_desc(addr, ATOM, 1024, 2);
+}
+
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmap, mla::FwdParams p) {
+  using L = Layout<kFp8>;
+  constexpr int NS = L::NS, NR = L::NR;
+  constexpr int OFF_STAGE = L::OFF_STAGE, OFF_RAW = L::OFF_RAW, OFF_QROPE = L::OFF_QROPE;
+  constexpr int OFF_RECV = L::OFF_RECV, OFF_BAR = L::OFF_BAR;
+  constexpr uint32_t kAB = kFp8 ? 0u : 1u;  // operand type: f16 (fp8 cache) or bf16
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Bars& bars = *reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const uint32_t sbase = ptx::smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int split = blockIdx.x >> 1, rb = blockIdx.y, b = blockIdx.z;
+
+  int ctx = p.seq_lens[b];
+  const int covered = p.num_splits * p.chunk_len;
+  if (ctx < 0 || ctx > covered) {
+    if (threadIdx.x == 0 && rank == 0) atomicOr(p.status, MLA_DEVFLAG_CTX_RANGE);
+    ctx = ctx < 0 ? 0 : covered;
+  }
+  const int k0 = split * p.chunk_len;
+  const int k1 = min(k0 + p.chunk_len, ctx);
+  const int n_tiles = k1 > k0 ? (k1 - k0 + T - 1) / T : 0;
+  const int vdim0 = (int)rank * 256;  // this CTA's value dims
+  const float s_kv = (p.kv_dtype == MLA_KV_FP8_E4M3 && p.kv_scale) ? *p.kv_scale : 1.f;
+
+  if (n_tiles == 0) {
+    // No key of this split: the row results are out = 0, lse = -inf.  Both
+    // CTAs of the pair take this branch together, before any cluster traffic.
+    for (int i = threadIdx.x; i < mla::kRowTile; i += kThreads) {
+      const int row = rb * mla::kRowTile + i;
+      if (row >= p.rows) break;
+      if (p.num_splits == 1) {
+        uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
+        for (int c = 0; c < 32; ++c) o[c] = make_uint4(0, 0, 0, 0);
+        if (rank == 0) p.lse[(size_t)b * p.rows + row] = -INFINITY;
+      } else if (rank == 0) {
+        p.part_lse[((size_t)b * p.num_splits + split) * p.rows + row] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), kFp8 ? 64 : 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < NR; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars.raw_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.raw_empty[s]), 64);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 128);
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i]), 128);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
+    ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
+    bars.abort = 0;
+    ptx::fence_mbar_init_cluster();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars.tmem_base), TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  Ctx c{p.status, &bars.abort};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loader ---
+    ptx::prefetch_tmap(&tmap);
+    const int n_slots = rank == 0 ? 5 : 4;
+    const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
+    auto key_row = [&](int tile) -> int2 {
+      // this lane's two keys of `tile` -> cache rows (clamped into the valid range)
+      const int start = k0 + tile * T;
+      const int last = min(T, k1 - start) - 1;
+      int2 rows;
+      for (int h = 0; h < 2; ++h) {
+        int kk = lane + 32 * h;
+        int j = start + min(kk, last);
+        int64_t page = bt[j / p.page_size];
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+          page = 0;
+        }
+        int r = (int)(page * p.page_size + j % p.page_size);
+        if (h == 0) rows.x = r; else rows.y = r;
+      }
+      return rows;
+    };
+    int2 rows = key_row(0);
+    int issued = 0;
+    // bf16: TMA straight into the swizzled operand stages.  fp8: TMA into the
+    // raw stages (64 B per key and slab), the dequant warps do the rest.
+    constexpr int NQ = kFp8 ? NR : NS;
+    const uint32_t slab = kFp8 ? ATOM8 : ATOM, row_bytes = kFp8 ? 64 : 128;
+    const uint32_t bytes = (uint32_t)n_slots * slab;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int s = t % NQ;
+      const uint32_t empty = ptx::smem_u32(kFp8 ? &bars.raw_empty[s] : &bars.kv_empty[s]);
+      if (t >= NQ && !wait_all<false>(c, empty, ((t / NQ) - 1) & 1)) break;
+      issued = t + 1;
+      const uint32_t full = ptx::smem_u32(kFp8 ? &bars.raw_full[s] : &bars.kv_full[s]);
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full, bytes);
+      __syncwarp();
+      const uint32_t dst = sbase + (kFp8 ? OFF_RAW + s * RAW_STAGE : OFF_STAGE + s * STAGE);
+      for (int sl = 0; sl < n_slots; ++sl) {
+        const int x = sl < 4 ? vdim0 + sl * 64 : 512;
+        ptx::tma_load_2d(dst + sl * slab + lane * row_bytes, &tmap, x, rows.x, full);
+        ptx::tma_load_2d(dst + sl * slab + (lane + 32) * row_bytes, &tmap, x, rows.y, full);
+      }
+      if (t + 1 < n_tiles) rows = key_row(t + 1);
+    }
+    if (*c.abort) {
+      // let the copies already in flight land before this CTA's memory goes away
+      for (int u = max(0, issued - NQ); u < issued; ++u)
+        wait_drain(ptx::smem_u32(kFp8 ? &bars.raw_full[u % NQ] : &bars.kv_full[u % NQ]),
+                   (u / NQ) & 1);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA ---
+    if (lane == 0) {
+      const uint32_t id_qk = ptx::idesc_f16(128, T, kAB, false, false);
+      const uint32_t id_pv = ptx::idesc_f16(128, 256, kAB, false, true);
+      bool ok = wait<false>(c, ptx::smem_u32(&bars.q_ready), 0);
+      ptx::tc_fence_after();
+      auto issue_qk = [&](int u) -> bool {
+        const int s = u % NS;
+        if (!wait<false>(c, ptx::smem_u32(&bars.kv_full[s]), (u / NS) & 1)) return false;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + TM_S + (u & 1) * T;
+        const uint32_t st = sbase + OFF_STAGE + s * STAGE;
+        for (int a = 0; a < 4; ++a)
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, kmajor_desc(st + a * ATOM + kk * 32),
+                        id_qk, (a | kk) != 0);
+        if (rank == 0) {
+          const uint32_t qr = sbase + OFF_QROPE;
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ss(d, kmajor_desc(qr + kk * 32), kmajor_desc(st + 4 * ATOM + kk * 32), id_qk, 1);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        if (t + 1 < n_tiles && !issue_qk(t + 1)) { ok = false; break; }
+        if (!wait<false>(c, ptx::smem_u32(&bars.p_full[t & 1]), (t >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t pa = tmem + TM_S + (t & 1) * T;
+        const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
+        for (int kk = 0; kk < T / 16; ++kk)
+          ptx::mma_ts(tmem + TM_O, pa + kk * 8, vmajor_desc(st + kk * 2048), id_pv, (t | kk) != 0);
+        ptx::mma_commit(ptx::smem_u32(&bars.o_done));
+        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
+      }
+      (void)ok;
+    }
+    __syncwarp();
+  } else if (warp == kDequantWarp0 || warp == kDequantWarp0 + 1) {
+    // ----------------------------------------------------------- dequant ---
+    // fp8 codes -> f16 operands in the 128B-swizzled K-major stage layout.
+    // The per-tensor scale is applied later (scores and output), so this is
+    // an exact format change.
+    if constexpr (kFp8) {
+    const int u0 = (warp - kDequantWarp0) * 32 + lane;  // 0..63
+    const int n_units = (rank == 0 ? 5 : 4) * T * 4;     // 16-code pieces per tile
+    for (int t = 0; t < n_tiles; ++t) {
+      const int sr = t % NR, so = t % NS;
+      if (!wait_all<false>(c, ptx::smem_u32(&bars.raw_full[sr]), (t / NR) & 1)) break;
+      if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[so]), ((t / NS) - 1) & 1)) break;
+      const uint32_t raw = sbase + OFF_RAW + sr * RAW_STAGE;
+      const uint32_t dst = sbase + OFF_STAGE + so * STAGE;
+      for (int u = u0; u < n_units; u += 64) {
+        const int sl = u / (T * 4), kk = (u >> 2) & (T - 1), piece = u & 3;
+        const uint4 codes = ld_shared_u4(raw + sl * ATOM8 + kk * 64 + piece * 16);
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_f16x2(codes.x);
+        lo.y = e4m3x2_to_f16x2(codes.x >> 16);
+        lo.z = e4m3x2_to_f16x2(codes.y);
+        lo.w = e4m3x2_to_f16x2(codes.y >> 16);
+        hi.x = e4m3x2_to_f16x2(codes.z);
+        hi.y = e4m3x2_to_f16x2(codes.z >> 16);
+        hi.z = e4m3x2_to_f16x2(codes.w);
+        hi.w = e4m3x2_to_f16x2(codes.w >> 16);
+        const uint32_t row = dst + sl * ATOM + kk * 128;
+        st_shared_u4(row + (((2 * piece) ^ (kk & 7)) * 16), lo);
+        st_shared_u4(row + (((2 * piece + 1) ^ (kk & 7)) * 16), hi);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.raw_empty[sr]));
+      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[so]));
+    }
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ----------------------------------------------------------- softmax ---
+    const int q4 = warp - kSoftmaxWarp0;       // TMEM lane quarter of this warp
+    const int r = q4 * 32 + lane;              // row within the 128-row block
+    const int row = rb * mla::kRowTile + r;    // row within the sequence
+    const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
+    const bool valid_row = row < p.rows;
+    int nvis = 0;
+    if (valid_row) {
+      const int tok = row / p.heads;
+      nvis = p.causal ? ctx - p.sq + tok + 1 : ctx;
+      nvis = max(0, min(nvis, ctx));
+    }
+    const int lim_all = min(nvis, k1);  // keys [k0, lim_all) are visible in this split
+
+    // Q (this CTA's 256 latent dims) -> TMEM as bf16 pairs; CTA 0 also puts
+    // the 64 rope dims into shared memory (128B-swizzled K-major).
+    {
+      const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.rows + row) * mla::kDQK);
+      uint32_t buf[32];
+      bool q_range = false;
+      for (int chunk = 0; chunk < 4; ++chunk) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 x = valid_row ? qv[(vdim0 + chunk * 64) / 8 + v] : make_uint4(0, 0, 0, 0);
+          if (kFp8) x = bf16x8_to_f16x8(x, q_range);
+          buf[v * 4 + 0] = x.x;
+          buf[v * 4 + 1] = x.y;
+          buf[v * 4 + 2] = x.z;
+          buf[v * 4 + 3] = x.w;
+        }
+        ptx::tmem_st32(tmem + lanes + TM_Q + chunk * 32, buf);
+      }
+      if (rank == 0) {
+        uint8_t* qr = smem + OFF_QROPE + r * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 x = valid_row ? qv[512 / 8 + v] : make_uint4(0, 0, 0, 0);
+          if (kFp8) x = bf16x8_to_f16x8(x, q_range);
+          *reinterpret_cast<uint4*>(qr + ((v ^ (r & 7)) * 16)) = x;
+        }
+        ptx::fence_proxy_async_smem();
+      }
+      if (kFp8 && q_range) atomicOr(p.status, MLA_DEVFLAG_Q_RANGE);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.q_ready));
+    }
+
+    const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
+    float m_run = kMaxSentinel, l_run = 0.f;
+    const uint32_t recv_local = sbase + OFF_RECV;
+    const uint32_t recv_peer = ptx::mapa(recv_local, peer);
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int buf = t & 1;
+      if (!wait_all<false>(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
+      ptx::tc_fence_after();
+      float s[T];
+      {
+        uint32_t raw[32];
+        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T, raw);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
+        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + 32, raw);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(raw[i]);
+      }
+      // swap partial scores with the partner CTA
+      const uint32_t my_off = (uint32_t)(buf * RECV + r * 16);
+#pragma unroll
+      for (int q = 0; q < T / 4; ++q)
+        ptx::st_cluster_v4(recv_peer + my_off + q * 128 * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
+                           s[4 * q + 3]);
+      ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer));
+      if (!wait_all<true>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
+#pragma unroll
+      for (int q = 0; q < T / 4; ++q) {
+        float4 v = ld_shared_v4(recv_local + my_off + q * 128 * 16);
+        s[4 * q] += v.x;
+        s[4 * q + 1] += v.y;
+        s[4 * q + 2] += v.z;
+        s[4 * q + 3] += v.w;
+      }
+      // mask and scale (log2 domain)
+      const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        s[i] = i < lim ? s[i] * c2 : -INFINITY;
+        mt = fmaxf(mt, s[i]);
+      }
+      const bool need = mt > m_run + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? fmaxf(m_run, mt) : m_run;
+        const float alpha = exp2f(m_run - m_new);
+        if (t > 0) {
+          // O must not be touched while PV(t-1) is still accumulating
+          if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(tmem + lanes + TM_O + ch * 32, o);
+          }
+          ptx::tmem_st_wait();
+        }
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      uint32_t pk[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < T / 2; ++i) {
+        const float p0 = exp2f(s[2 * i] - m_run);
+        const float p1 = exp2f(s[2 * i + 1] - m_run);
+        lsum += p0 + p1;
+        pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+      }
+      l_run += lsum;
+      ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
+    }
+
+    // ---------------------------------------------------------- epilogue ---
+    if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
+      ptx::tc_fence_after();
+      const float inv = l_run > 0.f ? s_kv / l_run : 0.f;
+      const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      const bool single = p.num_splits == 1;
+      uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
+      const size_t prow = ((size_t)b * p.num_splits + split) * p.rows + row;
+      float4* o_f32 = single ? nullptr : reinterpret_cast<float4*>(p.part_o + prow * mla::kDV + vdim0);
+#pragma unroll 1
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
+        ptx::tmem_ld_wait();
+        if (!valid_row) continue;
+        if (single) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            o_bf16[ch * 4 + v] = w;
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            o_f32[ch * 8 + v] =
+                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+        }
+      }
+      if (valid_row && rank == 0) {
+        if (single) p.lse[(size_t)b * p.rows + row] = lse;
+        else p.part_lse[prow] = lse;
+      }
+    }
+    ptx::tc_fence_before();
+  }
+
+  // ------------------------------------------------------------ teardown ---
+  __syncthreads();
+  if (warp == 1) {
+    if (bars.abort) {
+      // wait for every tcgen05 op this CTA issued before giving TMEM back
+      if (lane == 0) {
+        ptx::mma_commit(ptx::smem_u32(&bars.drain));
+        wait_drain(ptx::smem_u32(&bars.drain), 0);
+      }
+      __syncwarp();
+    }
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TM_COLS);
+  }
+  ptx::cluster_sync_all();  // no CTA leaves while its partner may still write into it
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled get_encode() {
+  static EncodeTiled fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
+  EncodeTiled encode = get_encode();
+  if (encode == nullptr) return (int)cudaErrorNotSupported;
+  const bool fp8 = p.kv_dtype == MLA_KV_FP8_E4M3;
+  CUtensorMap tmap;
+  const cuuint64_t rows_total = (cuuint64_t)p.num_pages * (cuuint64_t)p.page_size;
+  cuuint64_t dims[2] = {(cuuint64_t)mla::kDQK, rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)mla::kDQK * (fp8 ? 1 : 2)};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&tmap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      2, const_cast<void*>(p.cache), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+  auto kernel = fp8 ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
+  const int smem = fp8 ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[fp8]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    attr_done[fp8] = true;
+  }
+  dim3 grid(p.num_splits * 2, p.row_blocks, p.batch);
+  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(tmap, p);
+  return (int)cudaGetLastError();
+}
