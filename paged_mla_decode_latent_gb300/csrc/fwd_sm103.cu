@@ -9,8 +9,9 @@
 // 64 rope dims).  Each CTA therefore reads only its part of every latent row.
 //
 // Per 64-key tile, in each CTA:
-//   loader warp   : block-table lookup, one TMA box (64 dims x 1 row) per key
-//                   and per 64-dim atom into a 128B-swizzled K-major stage.
+//   loader warp   : block-table lookup, TMA gather of four key rows per
+//                   instruction (64 dims each) into a 128B-swizzled K-major
+//                   stage, one instruction per 4 keys and 64-dim slab.
 //   MMA warp      : S_part = Q_part K_part^T  (tcgen05, A = Q from TMEM,
 //                   CTA 0's rope part A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
@@ -296,31 +297,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmap);
     const int n_slots = rank == 0 ? 5 : 4;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
-    auto key_row = [&](int tile) -> int2 {
-      // this lane's two keys of `tile` -> cache rows (clamped into the valid range)
+    // Cache row of key j of this sequence, clamped into the valid range.
+    auto row_of = [&](int j) -> int {
+      int64_t page = bt[j / p.page_size];
+      if (page < 0 || page >= p.num_pages) {
+        atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+        page = 0;
+      }
+      return (int)(page * p.page_size + j % p.page_size);
+    };
+    // Lane l owns keys 4(l%16) .. 4(l%16)+3 of a tile; keys past the split's
+    // last key repeat that key (their scores are masked, their values are
+    // finite).  Lanes 0-15 copy the even slabs, lanes 16-31 the odd ones.
+    auto key_rows = [&](int tile) -> int4 {
       const int start = k0 + tile * T;
       const int last = min(T, k1 - start) - 1;
-      int2 rows;
-      for (int h = 0; h < 2; ++h) {
-        int kk = lane + 32 * h;
-        int j = start + min(kk, last);
-        int64_t page = bt[j / p.page_size];
-        if (page < 0 || page >= p.num_pages) {
-          atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-          page = 0;
-        }
-        int r = (int)(page * p.page_size + j % p.page_size);
-        if (h == 0) rows.x = r; else rows.y = r;
-      }
-      return rows;
+      const int kb = 4 * (lane & 15);
+      return make_int4(row_of(start + min(kb, last)), row_of(start + min(kb + 1, last)),
+                       row_of(start + min(kb + 2, last)), row_of(start + min(kb + 3, last)));
     };
-    int2 rows = key_row(0);
+    int4 rows = key_rows(0);
     int issued = 0;
     // bf16: TMA straight into the swizzled operand stages.  fp8: TMA into the
     // raw stages (64 B per key and slab), the dequant warps do the rest.
     constexpr int NQ = kFp8 ? NR : NS;
     const uint32_t slab = kFp8 ? ATOM8 : ATOM, row_bytes = kFp8 ? 64 : 128;
     const uint32_t bytes = (uint32_t)n_slots * slab;
+    const int kb = 4 * (lane & 15);
     for (int t = 0; t < n_tiles; ++t) {
       const int s = t % NQ;
       const uint32_t empty = ptx::smem_u32(kFp8 ? &bars.raw_empty[s] : &bars.kv_empty[s]);
@@ -330,12 +333,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
       const uint32_t dst = sbase + (kFp8 ? OFF_RAW + s * RAW_STAGE : OFF_STAGE + s * STAGE);
-      for (int sl = 0; sl < n_slots; ++sl) {
+      // Destinations are 4 rows = 256 B (fp8) or 512 B (bf16) apart from a
+      // 1 KB-aligned stage: tensor copies need 128-byte aligned shared memory.
+      for (int sl = lane >> 4; sl < n_slots; sl += 2) {
         const int x = sl < 4 ? vdim0 + sl * 64 : 512;
-        ptx::tma_load_2d(dst + sl * slab + lane * row_bytes, &tmap, x, rows.x, full);
-        ptx::tma_load_2d(dst + sl * slab + (lane + 32) * row_bytes, &tmap, x, rows.y, full);
+        ptx::tma_gather4(dst + sl * slab + kb * row_bytes, &tmap, x, rows.x, rows.y, rows.z,
+                         rows.w, full);
       }
-      if (t + 1 < n_tiles) rows = key_row(t + 1);
+      if (t + 1 < n_tiles) rows = key_rows(t + 1);
     }
     if (*c.abort) {
       // let the copies already in flight land before this CTA's memory goes away
