@@ -539,14 +539,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_run *= alpha;
         m_run = m_new;
       }
+      // The row sum adds the weights exactly as the PV MMA sees them (after
+      // rounding to 16 bits), so a dominant key's weight cancels in O / l.
       uint32_t pk[32];
       float lsum = 0.f;
 #pragma unroll
       for (int i = 0; i < T / 2; ++i) {
         const float p0 = exp2f(s[2 * i] - m_run);
         const float p1 = exp2f(s[2 * i + 1] - m_run);
-        lsum += p0 + p1;
-        pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+        if constexpr (kFp8) {
+          pk[i] = pack_f16(p0, p1);
+          const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+          lsum += r.x + r.y;
+        } else {
+          pk[i] = pack_bf16(p0, p1);
+          lsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+        }
       }
       l_run += lsum;
       ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);

@@ -2,9 +2,12 @@
 device, run the library through its C ABI, and compare with the fp64 oracle.
 
 Tolerances (bf16 output against the fp64 oracle on the same bits):
-  max |out - ref|                 <= 1.5e-2
-  ||out - ref||_F / ||ref||_F     <= 4e-3
-  max |lse - ref_lse|             <= 1e-3
+  max (|out - ref| - ulp_bf16(ref) / 2)   <= 1.5e-2
+  ||out - ref||_F / ||ref||_F             <= 4e-3
+  max |lse - ref_lse|                     <= 1e-3
+The max-abs bound is taken beyond the rounding of the exact value to bf16:
+the output format alone is off by up to half a bf16 ulp, which exceeds 1.5e-2
+once |ref| >= 4 (the MTP workload's x8 outlier rows give |out| near 30).
 Rows with no visible key must give out == 0 and lse == -inf exactly.
 """
 from __future__ import annotations
@@ -56,6 +59,13 @@ def oracle_full(p: syn.Problem, b_range=None):
                          p.seq_lens, p.softmax_scale, p.causal, b_range=b_range)
 
 
+def bf16_half_ulp(x):
+    """Half the spacing of bf16 numbers at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
 def assert_close(out, lse, ref_out, ref_lse, what=""):
     """The bar of the parity tests (see the module docstring)."""
     out = np.asarray(out, np.float64)
@@ -70,10 +80,11 @@ def assert_close(out, lse, ref_out, ref_lse, what=""):
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     err = np.abs(o - r)
     max_abs = float(err.max())
+    beyond = float((err - bf16_half_ulp(r)).max())
     fro = float(np.linalg.norm(o - r) / max(np.linalg.norm(r), 1e-30))
     lse_err = float(np.abs(lse[ok] - ref_lse[ok]).max())
-    stats = dict(max_abs=max_abs, rel_fro=fro, lse_abs=lse_err)
-    assert max_abs <= MAX_ABS, f"{what}: max abs {max_abs:.3e} > {MAX_ABS} {stats}"
+    stats = dict(max_abs=max_abs, beyond_rounding=beyond, rel_fro=fro, lse_abs=lse_err)
+    assert beyond <= MAX_ABS, f"{what}: max abs beyond bf16 rounding {beyond:.3e} > {MAX_ABS} {stats}"
     assert fro <= REL_FRO, f"{what}: rel Frobenius {fro:.3e} > {REL_FRO} {stats}"
     assert lse_err <= LSE_ABS, f"{what}: lse abs {lse_err:.3e} > {LSE_ABS} {stats}"
     return stats
