@@ -45,9 +45,9 @@ MI355X_HK_US = {"dense": 132.878}  # the pages' HK m16x8 time for this workload 
 
 # ------------------------------------------------------------------ workload ---
 
-def make_workload(name: str, seed: int = 0) -> syn.Problem:
+def make_workload(name: str, seed: int = 0, batch: int = 0, ctx: int = 0) -> syn.Problem:
     if name == "dense":
-        return syn.dense(64, 8192, seed=seed)
+        return syn.dense(batch or 64, ctx or 8192, seed=seed)
     if name == "ragged_bf16":
         return syn.ragged(syn.KV_BF16, seed=seed)
     if name == "ragged_fp8":
@@ -208,7 +208,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    p = make_workload(args.workload)
+    p = make_workload(args.workload, batch=args.batch, ctx=args.ctx)
     import oracle
     oracle.build()
     per_step = []
@@ -264,7 +264,7 @@ def run_gpu(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     mla.build()
-    p = make_workload(args.workload, seed=rank)
+    p = make_workload(args.workload, seed=rank, batch=args.batch, ctx=args.ctx)
     alg = algorithmic(p)
     t = to_device(p, dev)
     plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal)
@@ -362,7 +362,8 @@ def run_gpu(args):
 
     # end to end through the public API with host buffers: H2D of q, block
     # table and lengths from pinned memory, decode, D2H of out and lse
-    e2e = e2e_measure(mla, p, t, plan, ws, stream, dev, max(10, min(steps, 400)), world)
+    e2e = None if args.no_e2e else e2e_measure(mla, p, t, plan, ws, stream, dev,
+                                                max(10, min(steps, 400)), world)
 
     line = {
         "metric": METRIC, "value": kv_rate / 1e12, "unit": UNIT, "n_gpus": world,
@@ -447,7 +448,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense",
                     choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp"])
+    ap.add_argument("--batch", type=int, default=0, help="dense workload: batch (default 64)")
+    ap.add_argument("--ctx", type=int, default=0, help="dense workload: context (default 8192)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         if args.steps <= 0:

@@ -473,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
-    float m_run = kMaxSentinel, l_run = 0.f;
+    float m_run = kMaxSentinel, l_run = 0.f, l_rnd = 0.f;
     const uint32_t recv_local = sbase + OFF_RECV;
     const uint32_t recv_peer = ptx::mapa(recv_local, peer);
     bool ok = true;
@@ -537,26 +537,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::tmem_st_wait();
         }
         l_run *= alpha;
+        l_rnd *= alpha;
         m_run = m_new;
       }
-      // The row sum adds the weights exactly as the PV MMA sees them (after
-      // rounding to 16 bits), so a dominant key's weight cancels in O / l.
+      // Two row sums: the exact one gives the LSE; the other adds the
+      // weights as the PV MMA sees them (rounded to 16 bits) and normalises
+      // O, so a dominant key's rounding cancels in O / l.
       uint32_t pk[32];
-      float lsum = 0.f;
+      float lsum = 0.f, lsum_r = 0.f;
 #pragma unroll
       for (int i = 0; i < T / 2; ++i) {
         const float p0 = exp2f(s[2 * i] - m_run);
         const float p1 = exp2f(s[2 * i + 1] - m_run);
+        lsum += p0 + p1;
         if constexpr (kFp8) {
           pk[i] = pack_f16(p0, p1);
           const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-          lsum += r.x + r.y;
+          lsum_r += r.x + r.y;
         } else {
           pk[i] = pack_bf16(p0, p1);
-          lsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          lsum_r += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
         }
       }
       l_run += lsum;
+      l_rnd += lsum_r;
       ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -566,7 +570,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue ---
     if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
       ptx::tc_fence_after();
-      const float inv = l_run > 0.f ? s_kv / l_run : 0.f;
+      const float inv = l_rnd > 0.f ? s_kv / l_rnd : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       const bool single = p.num_splits == 1;
       uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
