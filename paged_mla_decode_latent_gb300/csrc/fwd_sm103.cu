@@ -17,10 +17,11 @@
 //                   O_half += P V_half        (A = P from TMEM, B = the same
 //                   stage read MN-major as V).
 //   softmax warps : read S_part from TMEM, swap it with the partner CTA over
-//                   distributed shared memory, add (identical order in both
-//                   CTAs, so both see bit-identical scores), mask, online
-//                   softmax with a lazily rescaled running max, P -> TMEM as
-//                   bf16 over the consumed score columns.
+//                   distributed shared memory (st.async counted on the
+//                   partner's mbarrier), add (identical order in both CTAs,
+//                   so both see bit-identical scores), mask, online softmax
+//                   with a lazily rescaled running max, P -> TMEM over the
+//                   consumed score columns (bf16 as a high + low pair).
 // The epilogue normalises O and writes bf16 output (one split) or fp32
 // partials plus the per-row log-sum-exp (several splits).
 //
@@ -82,7 +83,8 @@ static_assert(Layout<true>::SMEM_BYTES <= 232448, "fp8 smem");
 // TMEM columns
 constexpr uint32_t TM_O = 0;     // 256 fp32 columns: this CTA's value half
 constexpr uint32_t TM_Q = 256;   // 128 columns: 256 bf16 of Q, packed in pairs
-constexpr uint32_t TM_S = 384;   // two 64-column score buffers; P overwrites cols 0..31
+constexpr uint32_t TM_S = 384;   // two 64-column score buffers; P overwrites them (bf16:
+                                 // cols 0..31 high-order, 32..63 low-order weights)
 constexpr uint32_t TM_COLS = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before a rescale
@@ -274,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 128);
-      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i]), 128);
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
@@ -382,6 +384,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
         for (int kk = 0; kk < T / 16; ++kk)
           ptx::mma_ts(tmem + TM_O, pa + kk * 8, vmajor_desc(st + kk * 2048), id_pv, (t | kk) != 0);
+        if constexpr (!kFp8) {  // second-order weights (see the softmax)
+          for (int kk = 0; kk < T / 16; ++kk)
+            ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, vmajor_desc(st + kk * 2048), id_pv, 1);
+        }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
         ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
       }
@@ -493,14 +499,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(raw[i]);
       }
-      // swap partial scores with the partner CTA
+      // Swap partial scores with the partner CTA: asynchronous remote stores
+      // that count their bytes on the partner's recv_full barrier, whose
+      // arrival is this CTA's own expect_tx of the 32 KB it will receive.
       const uint32_t my_off = (uint32_t)(buf * RECV + r * 16);
+      const uint32_t peer_bar = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer);
 #pragma unroll
       for (int q = 0; q < T / 4; ++q)
-        ptx::st_cluster_v4(recv_peer + my_off + q * 128 * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
-                           s[4 * q + 3]);
-      ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer));
-      if (!wait_all<true>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
+        ptx::st_async_v4(recv_peer + my_off + q * 128 * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
+                         s[4 * q + 3], peer_bar);
+      if (r == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars.recv_full[buf]), RECV);
+      if (!wait_all<false>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
 #pragma unroll
       for (int q = 0; q < T / 4; ++q) {
         float4 v = ld_shared_v4(recv_local + my_off + q * 128 * 16);
@@ -540,28 +549,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_rnd *= alpha;
         m_run = m_new;
       }
-      // Two row sums: the exact one gives the LSE; the other adds the
-      // weights as the PV MMA sees them (rounded to 16 bits) and normalises
-      // O, so a dominant key's rounding cancels in O / l.
+      // Weights for PV.  bf16 keeps 8 significant bits, so a weight is also
+      // written as a second bf16 term holding what the first one rounded
+      // away (P = P_hi + P_lo to ~16 bits); the MMA warp accumulates both.
+      // f16 (fp8 cache) keeps 11 bits and needs no second term.  Two row
+      // sums: the exact one gives the LSE, the other adds the weights as the
+      // MMAs see them and normalises O, so a dominant key's rounding cancels.
       uint32_t pk[32];
       float lsum = 0.f, lsum_r = 0.f;
+      if constexpr (kFp8) {
 #pragma unroll
-      for (int i = 0; i < T / 2; ++i) {
-        const float p0 = exp2f(s[2 * i] - m_run);
-        const float p1 = exp2f(s[2 * i + 1] - m_run);
-        lsum += p0 + p1;
-        if constexpr (kFp8) {
+        for (int i = 0; i < T / 2; ++i) {
+          const float p0 = exp2f(s[2 * i] - m_run);
+          const float p1 = exp2f(s[2 * i + 1] - m_run);
+          lsum += p0 + p1;
           pk[i] = pack_f16(p0, p1);
-          const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-          lsum_r += r.x + r.y;
-        } else {
-          pk[i] = pack_bf16(p0, p1);
-          lsum_r += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          const float2 rr = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+          lsum_r += rr.x + rr.y;
         }
+        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
+      } else {
+        uint32_t pl[32];
+#pragma unroll
+        for (int i = 0; i < T / 2; ++i) {
+          const float p0 = exp2f(s[2 * i] - m_run);
+          const float p1 = exp2f(s[2 * i + 1] - m_run);
+          lsum += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+          const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
+          pl[i] = pack_bf16(p0 - h0, p1 - h1);
+          lsum_r += (h0 + __uint_as_float(pl[i] << 16)) + (h1 + __uint_as_float(pl[i] & 0xFFFF0000u));
+        }
+        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
+        ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
       }
       l_run += lsum;
       l_rnd += lsum_r;
-      ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));

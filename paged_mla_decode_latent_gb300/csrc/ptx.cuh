@@ -236,6 +236,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, fl
                : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory that counts
+// its bytes on an mbarrier of that CTA (complete_tx); needs no fence.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
+                                            float d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
