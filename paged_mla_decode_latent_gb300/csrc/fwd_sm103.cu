@@ -357,10 +357,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = ptx::idesc_f16(128, 256, kAB, false, true);
       bool ok = wait<false>(c, ptx::smem_u32(&bars.q_ready), 0);
       ptx::tc_fence_after();
-      auto issue_qk = [&](int u) -> bool {
+      auto issue_qk = [&](int u) {
         const int s = u % NS;
-        if (!wait<false>(c, ptx::smem_u32(&bars.kv_full[s]), (u / NS) & 1)) return false;
-        ptx::tc_fence_after();
         const uint32_t d = tmem + TM_S + (u & 1) * T;
         const uint32_t st = sbase + OFF_STAGE + s * STAGE;
         for (int a = 0; a < 4; ++a)
@@ -373,13 +371,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mma_ss(d, kmajor_desc(qr + kk * 32), kmajor_desc(st + 4 * ATOM + kk * 32), id_qk, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
-        return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        if (t + 1 < n_tiles && !issue_qk(t + 1)) { ok = false; break; }
-        if (!wait<false>(c, ptx::smem_u32(&bars.p_full[t & 1]), (t >> 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
+      auto issue_pv = [&](int t) {
         const uint32_t pa = tmem + TM_S + (t & 1) * T;
         const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
         for (int kk = 0; kk < T / 16; ++kk)
@@ -390,6 +383,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
         ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
+      };
+      // Issue whichever is ready: QK^T of tile nq (its stage has landed and
+      // its score buffer is free, i.e. the PV of tile nq-2 is issued; the
+      // tensor pipe runs one thread's MMAs in order) or PV of tile np (its
+      // weights are written).  A late stage never holds back a ready PV.
+      int nq = 0, np = 0;
+      uint64_t t_last = ptx::globaltimer_ns();
+      uint32_t idle = 0;
+      while (ok && np < n_tiles) {
+        bool progress = false;
+        if (nq < n_tiles && nq <= np + 1 &&
+            ptx::mbar_test_wait(ptx::smem_u32(&bars.kv_full[nq % NS]), (nq / NS) & 1)) {
+          ptx::tc_fence_after();
+          issue_qk(nq++);
+          progress = true;
+        }
+        if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1)) {
+          ptx::tc_fence_after();
+          issue_pv(np++);
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+          t_last = 0;
+        } else if ((++idle & 255) == 0) {
+          const uint64_t now = ptx::globaltimer_ns();
+          if (t_last == 0) t_last = now;
+          if (*c.abort) ok = false;
+          else if (now - t_last > kTimeoutNs) {
+            atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
+            *c.abort = 1;
+            ok = false;
+          }
+        }
       }
       (void)ok;
     }
