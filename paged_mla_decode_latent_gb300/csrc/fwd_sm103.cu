@@ -102,8 +102,10 @@ struct Bars {
   uint64_t o_done;
   uint64_t q_ready;
   uint64_t drain;
+  uint64_t heavy_bar[2];  // bf16: the four softmax warps' votes are in
   uint32_t tmem_base;
   int32_t abort;
+  uint32_t heavy[2];  // bf16: per score buffer, one byte per softmax warp (see the softmax)
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -281,6 +283,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars.heavy_bar[0]), 4);
+    ptx::mbar_init(ptx::smem_u32(&bars.heavy_bar[1]), 4);
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
   }
@@ -299,35 +303,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmap);
     const int n_slots = rank == 0 ? 5 : 4;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
-    // Cache row of key j of this sequence, clamped into the valid range.
-    auto row_of = [&](int j) -> int {
-      int64_t page = bt[j / p.page_size];
-      if (page < 0 || page >= p.num_pages) {
-        atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-        page = 0;
-      }
-      return (int)(page * p.page_size + j % p.page_size);
-    };
     // Lane l owns keys 4(l%16) .. 4(l%16)+3 of a tile; keys past the split's
     // last key repeat that key (their scores are masked, their values are
     // finite).  Lanes 0-15 copy the even slabs, lanes 16-31 the odd ones.
-    auto key_rows = [&](int tile) -> int4 {
+    // Block-table entries are read two tiles ahead (plain independent loads,
+    // no dependence between them) and range-checked only when used, so the
+    // table's latency stays off the copy path.
+    const int kb = 4 * (lane & 15);
+    auto key_of = [&](int tile, int i) -> int {
       const int start = k0 + tile * T;
-      const int last = min(T, k1 - start) - 1;
-      const int kb = 4 * (lane & 15);
-      return make_int4(row_of(start + min(kb, last)), row_of(start + min(kb + 1, last)),
-                       row_of(start + min(kb + 2, last)), row_of(start + min(kb + 3, last)));
+      return start + min(kb + i, min(T, k1 - start) - 1);
     };
-    int4 rows = key_rows(0);
+    auto load_pages = [&](int tile, int (&pg)[4]) {
+      if (tile >= n_tiles) return;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pg[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
+    };
+    auto rows_of = [&](int tile, const int (&pg)[4]) -> int4 {
+      int r[4];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int64_t page = pg[i];
+        if (page < 0 || page >= p.num_pages) {
+          bad = true;
+          page = 0;
+        }
+        r[i] = (int)(page * p.page_size + key_of(tile, i) % p.page_size);
+      }
+      if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+      return make_int4(r[0], r[1], r[2], r[3]);
+    };
+    int pg_cur[4] = {0, 0, 0, 0}, pg_next[4] = {0, 0, 0, 0};
+    load_pages(0, pg_cur);
+    load_pages(1, pg_next);
     int issued = 0;
     // bf16: TMA straight into the swizzled operand stages.  fp8: TMA into the
     // raw stages (64 B per key and slab), the dequant warps do the rest.
     constexpr int NQ = kFp8 ? NR : NS;
     const uint32_t slab = kFp8 ? ATOM8 : ATOM, row_bytes = kFp8 ? 64 : 128;
     const uint32_t bytes = (uint32_t)n_slots * slab;
-    const int kb = 4 * (lane & 15);
     for (int t = 0; t < n_tiles; ++t) {
       const int s = t % NQ;
+      const int4 rows = rows_of(t, pg_cur);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pg_cur[i] = pg_next[i];
+      load_pages(t + 2, pg_next);
       const uint32_t empty = ptx::smem_u32(kFp8 ? &bars.raw_empty[s] : &bars.kv_empty[s]);
       if (t >= NQ && !wait_all<false>(c, empty, ((t / NQ) - 1) & 1)) break;
       issued = t + 1;
@@ -342,7 +363,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tma_gather4(dst + sl * slab + kb * row_bytes, &tmap, x, rows.x, rows.y, rows.z,
                          rows.w, full);
       }
-      if (t + 1 < n_tiles) rows = key_rows(t + 1);
     }
     if (*c.abort) {
       // let the copies already in flight land before this CTA's memory goes away
@@ -372,12 +392,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
       };
-      auto issue_pv = [&](int t) {
+      auto issue_pv = [&](int t, bool second) {
         const uint32_t pa = tmem + TM_S + (t & 1) * T;
         const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
         for (int kk = 0; kk < T / 16; ++kk)
           ptx::mma_ts(tmem + TM_O, pa + kk * 8, vmajor_desc(st + kk * 2048), id_pv, (t | kk) != 0);
-        if constexpr (!kFp8) {  // second-order weights (see the softmax)
+        if (!kFp8 && second) {  // second-order weights (see the softmax)
           for (int kk = 0; kk < T / 16; ++kk)
             ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, vmajor_desc(st + kk * 2048), id_pv, 1);
         }
@@ -401,7 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1)) {
           ptx::tc_fence_after();
-          issue_pv(np++);
+          const bool second = *reinterpret_cast<volatile uint32_t*>(&bars.heavy[np & 1]) != 0;
+          issue_pv(np++, second);
           progress = true;
         }
         if (progress) {
@@ -506,7 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
-    float m_run = kMaxSentinel, l_run = 0.f, l_rnd = 0.f;
+    float m_run = kMaxSentinel, l_run = 0.f;
     const uint32_t recv_local = sbase + OFF_RECV;
     const uint32_t recv_peer = ptx::mapa(recv_local, peer);
     bool ok = true;
@@ -545,14 +566,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s[4 * q + 2] += v.z;
         s[4 * q + 3] += v.w;
       }
-      // mask and scale (log2 domain)
+      // Row max over the visible keys of this tile (log2 domain).  Only the
+      // last tile of a split and causal rows need the mask.
       const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
-      float mt = -INFINITY;
+      const bool full_tile = lim >= T;
+      float mt_raw = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < T; ++i) {
-        s[i] = i < lim ? s[i] * c2 : -INFINITY;
-        mt = fmaxf(mt, s[i]);
-      }
+      for (int i = 0; i < T; ++i)
+        if (full_tile || i < lim) mt_raw = fmaxf(mt_raw, s[i]);
+      const float mt = lim > 0 ? mt_raw * c2 : -INFINITY;
       const bool need = mt > m_run + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? fmaxf(m_run, mt) : m_run;
@@ -573,45 +595,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::tmem_st_wait();
         }
         l_run *= alpha;
-        l_rnd *= alpha;
         m_run = m_new;
       }
-      // Weights for PV.  bf16 keeps 8 significant bits, so a weight is also
-      // written as a second bf16 term holding what the first one rounded
-      // away (P = P_hi + P_lo to ~16 bits); the MMA warp accumulates both.
-      // f16 (fp8 cache) keeps 11 bits and needs no second term.  Two row
-      // sums: the exact one gives the LSE, the other adds the weights as the
-      // MMAs see them and normalises O, so a dominant key's rounding cancels.
+      // Weights p = 2^(s*c2 - m) (s now holds them), written as 16-bit pairs
+      // over the consumed score columns.  The row sum is exact (fp32).
+      const float neg_m = -m_run;
       uint32_t pk[32];
-      float lsum = 0.f, lsum_r = 0.f;
-      if constexpr (kFp8) {
+      float lsum = 0.f;
 #pragma unroll
-        for (int i = 0; i < T / 2; ++i) {
-          const float p0 = exp2f(s[2 * i] - m_run);
-          const float p1 = exp2f(s[2 * i + 1] - m_run);
-          lsum += p0 + p1;
-          pk[i] = pack_f16(p0, p1);
-          const float2 rr = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-          lsum_r += rr.x + rr.y;
+      for (int i = 0; i < T / 2; ++i) {
+        float p0 = exp2f(fmaf(s[2 * i], c2, neg_m));
+        float p1 = exp2f(fmaf(s[2 * i + 1], c2, neg_m));
+        if (!full_tile) {
+          p0 = 2 * i < lim ? p0 : 0.f;
+          p1 = 2 * i + 1 < lim ? p1 : 0.f;
         }
-        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
-      } else {
-        uint32_t pl[32];
-#pragma unroll
-        for (int i = 0; i < T / 2; ++i) {
-          const float p0 = exp2f(s[2 * i] - m_run);
-          const float p1 = exp2f(s[2 * i + 1] - m_run);
-          lsum += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-          const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-          pl[i] = pack_bf16(p0 - h0, p1 - h1);
-          lsum_r += (h0 + __uint_as_float(pl[i] << 16)) + (h1 + __uint_as_float(pl[i] & 0xFFFF0000u));
-        }
-        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
-        ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
+        s[2 * i] = p0;
+        s[2 * i + 1] = p1;
+        lsum += p0 + p1;
+        pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
       }
       l_run += lsum;
-      l_rnd += lsum_r;
+      ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
+      if constexpr (!kFp8) {
+        // bf16 keeps 8 significant bits.  Where one key carries a sizeable
+        // share of a row's weight (more than 1/64 of the row sum so far), the
+        // rounding would show in O, so the tile also gets a second bf16 term
+        // with what the first rounded away (P = P_hi + P_lo to ~16 bits) and
+        // the MMA warp adds a second PV.  Elsewhere the rounding errors of
+        // many small weights average out.  The decision is per tile for the
+        // whole CTA (one byte per warp, gathered on an mbarrier).
+        const float pmax = lim > 0 ? exp2f(mt - m_run) : 0.f;
+        const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
+        if (lane == 0) {
+          reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
+          ptx::mbar_arrive(ptx::smem_u32(&bars.heavy_bar[buf]));
+        }
+        if (!wait_all<false>(c, ptx::smem_u32(&bars.heavy_bar[buf]), (t >> 1) & 1)) { ok = false; break; }
+        if (*reinterpret_cast<volatile uint32_t*>(&bars.heavy[buf]) != 0) {
+          uint32_t pl[32];
+#pragma unroll
+          for (int i = 0; i < T / 2; ++i) {
+            const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
+            pl[i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
+          }
+          ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
+        }
+      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
@@ -620,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue ---
     if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
       ptx::tc_fence_after();
-      const float inv = l_rnd > 0.f ? s_kv / l_rnd : 0.f;
+      const float inv = l_run > 0.f ? s_kv / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       const bool single = p.num_splits == 1;
       uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
