@@ -200,6 +200,45 @@ int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens,
 int mla_decode_check(const mla_decode_plan_t* plan, const void* workspace, void* stream,
                      int32_t* host_status);
 
+/*
+ * mla_decode_fwd_noalloc -- mla_decode_fwd followed by mla_decode_combine,
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this call.
+ *
+ * Who needs it: a plugin inside a server or framework whose host owns all
+ * device memory through its own pool (a private cudaMalloc would bypass that
+ * pool and its budget), or a latency-critical loop that must not call
+ * cudaMalloc / cudaFree, which can synchronise the device.  Such a caller
+ * cannot hand over a workspace; here the library uses its own scratch array.
+ *
+ * Arguments: as mla_decode_fwd, without workspace and workspace_bytes; the
+ * caller still passes every input and both outputs.  out and lse are final on
+ * return of the queued work (the combine is queued here too).
+ *
+ * Scratch: one fixed 64 MiB device array inside this library, created on
+ * every GPU that loads it and held until the process exits.  Plans whose
+ * plan->workspace_bytes exceed 64 MiB are rejected with MLA_ERR_WORKSPACE
+ * (roughly batch * num_splits * H * Sq <= 32768 partial rows); a one-split
+ * plan always fits.  The first call on each device looks the array's device
+ * address up (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture.  Nothing is allocated or
+ * freed, by this call or by anything it calls.
+ *
+ * All calls share the one array and it keeps the previous call's contents;
+ * everything that must start at zero is reset on each call.  Calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * the array: serialise them.  With no caller workspace there is no status
+ * word to read back (mla_decode_check does not apply); out-of-range page ids
+ * and contexts are still clamped on the device, never faulted.
+ *
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE (plan too large for
+ * the scratch), MLA_ERR_UNSUPPORTED (device ordinal >= 64) or MLA_ERR_CUDA.
+ */
+int mla_decode_fwd_noalloc(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
+                           int64_t num_pages, const float* kv_scale, const int32_t* block_table,
+                           int64_t bt_stride, const int32_t* seq_lens, float softmax_scale,
+                           void* out, float* lse, void* stream);
+
 /* Static text for a status code. */
 const char* mla_status_string(int status);
 

@@ -40,7 +40,8 @@ DEVFLAG_Q_RANGE = 0x8
 
 # Every symbol include/mla_decode.h declares.
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_fwd", "mla_decode_combine",
-                    "mla_decode_check", "mla_status_string", "mla_decode_version")
+                    "mla_decode_check", "mla_decode_fwd_noalloc", "mla_status_string",
+                    "mla_decode_version")
 
 
 class Plan(ctypes.Structure):
@@ -88,6 +89,8 @@ def lib():
     L.mla_decode_fwd.restype = ctypes.c_int
     L.mla_decode_combine.argtypes = [P, vp, vp, ctypes.c_size_t, vp, vp, vp]
     L.mla_decode_combine.restype = ctypes.c_int
+    L.mla_decode_fwd_noalloc.argtypes = [P, vp, vp, i64, vp, vp, i64, vp, f32, vp, vp, vp]
+    L.mla_decode_fwd_noalloc.restype = ctypes.c_int
     L.mla_decode_check.argtypes = [P, vp, vp, ctypes.POINTER(i32)]
     L.mla_decode_check.restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
