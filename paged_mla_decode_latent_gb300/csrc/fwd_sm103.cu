@@ -9,9 +9,12 @@
 // 64 rope dims).  Each CTA therefore reads only its part of every latent row.
 //
 // Per 64-key tile, in each CTA:
-//   loader warp   : block-table lookup, TMA gather of four key rows per
-//                   instruction (64 dims each) into a 128B-swizzled K-major
-//                   stage, one instruction per 4 keys and 64-dim slab.
+//   loader warps  : block-table lookup one tile ahead, 16-byte cp.async of
+//                   the tile's rows in 128-byte pieces (one 64-dim slab of one
+//                   key) straight into a 128B-swizzled K-major stage (bf16),
+//                   or into a raw stage that the same threads convert to f16
+//                   (fp8); each thread fences its own copies for the tensor
+//                   cores and arrives on the stage's barrier.
 //   MMA warp      : S_part = Q_part K_part^T  (tcgen05, A = Q from TMEM,
 //                   CTA 0's rope part A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
@@ -38,7 +41,6 @@
 // MLA_DEVFLAG_TIMEOUT in the status word and the CTA winds down instead of
 // hanging the GPU.
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -60,16 +62,16 @@ constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
 constexpr int RECV = 128 * T * 4;      // one partner score tile, fp32
 constexpr int kThreads = 256;
-constexpr int kDequantWarp0 = 2;       // fp8 cache: warps 2-3 turn codes into f16
+constexpr int kLoadWarp0 = 2;          // warps 2-3 copy the cache rows
 constexpr int kSoftmaxWarp0 = 4;
 
-// Shared-memory plan.  bf16 cache: 3 operand stages filled by TMA.  fp8
-// cache: 3 raw stages filled by TMA + 2 f16 operand stages filled by the
-// dequant warps.
+// Shared-memory plan.  bf16 cache: 3 operand stages the loader warps fill
+// with cp.async.  fp8 cache: 2 raw stages of codes (cp.async) + 2 f16 operand
+// stages the same loader threads convert into.
 template <bool kFp8>
 struct Layout {
   static constexpr int NS = kFp8 ? 2 : 3;   // operand stages (what the MMA reads)
-  static constexpr int NR = kFp8 ? 3 : 0;   // raw fp8 stages
+  static constexpr int NR = kFp8 ? 2 : 0;   // raw fp8 stages
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
@@ -92,10 +94,8 @@ constexpr float kMaxSentinel = -1.0e30f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 struct Bars {
-  uint64_t kv_full[3];    // operand stage ready (TMA bytes landed / dequant done)
+  uint64_t kv_full[3];    // operand stage ready (64 loader threads arrive)
   uint64_t kv_empty[3];   // operand stage consumed by the MMAs
-  uint64_t raw_full[3];   // fp8: raw stage landed
-  uint64_t raw_empty[3];  // fp8: raw stage converted
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t recv_full[2];
@@ -220,7 +220,7 @@ __device__ __forceinline__ uint64_t vmajor_desc(uint32_t addr) {
 
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmap, mla::FwdParams p) {
+    fwd_sm103_kernel(mla::FwdParams p) {
   using L = Layout<kFp8>;
   constexpr int NS = L::NS, NR = L::NR;
   constexpr int OFF_STAGE = L::OFF_STAGE, OFF_RAW = L::OFF_RAW, OFF_QROPE = L::OFF_QROPE;
@@ -268,12 +268,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), kFp8 ? 64 : 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 64);
       ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s]), 1);
-    }
-    for (int s = 0; s < NR; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars.raw_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars.raw_empty[s]), 64);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
@@ -298,79 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ loader ---
-    ptx::prefetch_tmap(&tmap);
-    const int n_slots = rank == 0 ? 5 : 4;
-    const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
-    // Lane l owns keys 4(l%16) .. 4(l%16)+3 of a tile; keys past the split's
-    // last key repeat that key (their scores are masked, their values are
-    // finite).  Lanes 0-15 copy the even slabs, lanes 16-31 the odd ones.
-    // Block-table entries are read two tiles ahead (plain independent loads,
-    // no dependence between them) and range-checked only when used, so the
-    // table's latency stays off the copy path.
-    const int kb = 4 * (lane & 15);
-    auto key_of = [&](int tile, int i) -> int {
-      const int start = k0 + tile * T;
-      return start + min(kb + i, min(T, k1 - start) - 1);
-    };
-    auto load_pages = [&](int tile, int (&pg)[4]) {
-      if (tile >= n_tiles) return;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pg[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
-    };
-    auto rows_of = [&](int tile, const int (&pg)[4]) -> int4 {
-      int r[4];
-      bool bad = false;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        int64_t page = pg[i];
-        if (page < 0 || page >= p.num_pages) {
-          bad = true;
-          page = 0;
-        }
-        r[i] = (int)(page * p.page_size + key_of(tile, i) % p.page_size);
-      }
-      if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-      return make_int4(r[0], r[1], r[2], r[3]);
-    };
-    int pg_cur[4] = {0, 0, 0, 0}, pg_next[4] = {0, 0, 0, 0};
-    load_pages(0, pg_cur);
-    load_pages(1, pg_next);
-    int issued = 0;
-    // bf16: TMA straight into the swizzled operand stages.  fp8: TMA into the
-    // raw stages (64 B per key and slab), the dequant warps do the rest.
-    constexpr int NQ = kFp8 ? NR : NS;
-    const uint32_t slab = kFp8 ? ATOM8 : ATOM, row_bytes = kFp8 ? 64 : 128;
-    const uint32_t bytes = (uint32_t)n_slots * slab;
-    for (int t = 0; t < n_tiles; ++t) {
-      const int s = t % NQ;
-      const int4 rows = rows_of(t, pg_cur);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pg_cur[i] = pg_next[i];
-      load_pages(t + 2, pg_next);
-      const uint32_t empty = ptx::smem_u32(kFp8 ? &bars.raw_empty[s] : &bars.kv_empty[s]);
-      if (t >= NQ && !wait_all<false>(c, empty, ((t / NQ) - 1) & 1)) break;
-      issued = t + 1;
-      const uint32_t full = ptx::smem_u32(kFp8 ? &bars.raw_full[s] : &bars.kv_full[s]);
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full, bytes);
-      __syncwarp();
-      const uint32_t dst = sbase + (kFp8 ? OFF_RAW + s * RAW_STAGE : OFF_STAGE + s * STAGE);
-      // Destinations are 4 rows = 256 B (fp8) or 512 B (bf16) apart from a
-      // 1 KB-aligned stage: tensor copies need 128-byte aligned shared memory.
-      for (int sl = lane >> 4; sl < n_slots; sl += 2) {
-        const int x = sl < 4 ? vdim0 + sl * 64 : 512;
-        ptx::tma_gather4(dst + sl * slab + kb * row_bytes, &tmap, x, rows.x, rows.y, rows.z,
-                         rows.w, full);
-      }
-    }
-    if (*c.abort) {
-      // let the copies already in flight land before this CTA's memory goes away
-      for (int u = max(0, issued - NQ); u < issued; ++u)
-        wait_drain(ptx::smem_u32(kFp8 ? &bars.raw_full[u % NQ] : &bars.kv_full[u % NQ]),
-                   (u / NQ) & 1);
-    }
-  } else if (warp == 1) {
+  if (warp == 1) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
       const uint32_t id_qk = ptx::idesc_f16(128, T, kAB, false, false);
@@ -442,41 +366,115 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (warp == kDequantWarp0 || warp == kDequantWarp0 + 1) {
-    // ----------------------------------------------------------- dequant ---
-    // fp8 codes -> f16 operands in the 128B-swizzled K-major stage layout.
-    // The per-tensor scale is applied later (scores and output), so this is
-    // an exact format change.
-    if constexpr (kFp8) {
-    const int u0 = (warp - kDequantWarp0) * 32 + lane;  // 0..63
-    const int n_units = (rank == 0 ? 5 : 4) * T * 4;     // 16-code pieces per tile
-    for (int t = 0; t < n_tiles; ++t) {
-      const int sr = t % NR, so = t % NS;
-      if (!wait_all<false>(c, ptx::smem_u32(&bars.raw_full[sr]), (t / NR) & 1)) break;
-      if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[so]), ((t / NS) - 1) & 1)) break;
-      const uint32_t raw = sbase + OFF_RAW + sr * RAW_STAGE;
-      const uint32_t dst = sbase + OFF_STAGE + so * STAGE;
-      for (int u = u0; u < n_units; u += 64) {
-        const int sl = u / (T * 4), kk = (u >> 2) & (T - 1), piece = u & 3;
-        const uint4 codes = ld_shared_u4(raw + sl * ATOM8 + kk * 64 + piece * 16);
-        uint4 lo, hi;
-        lo.x = e4m3x2_to_f16x2(codes.x);
-        lo.y = e4m3x2_to_f16x2(codes.x >> 16);
-        lo.z = e4m3x2_to_f16x2(codes.y);
-        lo.w = e4m3x2_to_f16x2(codes.y >> 16);
-        hi.x = e4m3x2_to_f16x2(codes.z);
-        hi.y = e4m3x2_to_f16x2(codes.z >> 16);
-        hi.z = e4m3x2_to_f16x2(codes.w);
-        hi.w = e4m3x2_to_f16x2(codes.w >> 16);
-        const uint32_t row = dst + sl * ATOM + kk * 128;
-        st_shared_u4(row + (((2 * piece) ^ (kk & 7)) * 16), lo);
-        st_shared_u4(row + (((2 * piece + 1) ^ (kk & 7)) * 16), hi);
+  } else if (warp == kLoadWarp0 || warp == kLoadWarp0 + 1) {
+    // ------------------------------------------------------------ loader ---
+    // Gather of the tile's cache rows with 16-byte cp.async (L2 only).  The
+    // operand layout keeps a key's 64-dim slab contiguous only over 128 B, so
+    // every copy is a 128-byte piece of one row: 8 lanes per (key, slab)
+    // piece for bf16 (written straight into the 128B-swizzled stage), 4 lanes
+    // per 64-byte piece of fp8 codes (into a raw stage, converted below by
+    // the thread that copied it).  Thread (warp w, lane l) always serves the
+    // same NK keys of a tile, so it needs NK block-table entries per tile,
+    // read one tile ahead.  Each thread retires tile t-1 after issuing tile
+    // t: waits for its own copies, converts (fp8), fences them for the
+    // tensor cores' async proxy and arrives on the stage's full barrier.
+    constexpr int LPI = kFp8 ? 4 : 8;        // lanes per piece
+    constexpr int IPI = 32 / LPI;            // pieces per warp instruction
+    constexpr int NK = T / (2 * IPI);        // keys per thread: 8 (bf16) or 4 (fp8)
+    const int lw = warp - kLoadWarp0, g = lane / LPI, sub = lane % LPI;
+    const int n_slots = rank == 0 ? 5 : 4;
+    const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
+    const char* cache = static_cast<const char*>(p.cache);
+    auto key_of = [&](int tile, int i) -> int {  // i-th key of this thread, clamped to the split
+      const int start = k0 + tile * T;
+      const int kk = i * 2 * IPI + lw * IPI + g;
+      return start + min(kk, min(T, k1 - start) - 1);
+    };
+    int pg_next[NK];
+    auto load_pages = [&](int tile) {
+      if (tile >= n_tiles) return;
+#pragma unroll
+      for (int i = 0; i < NK; ++i) pg_next[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
+    };
+    load_pages(0);
+    bool ok = true;
+    for (int t = 0; t <= n_tiles; ++t) {
+      if (t < n_tiles) {
+        const int s = t % NS;
+        // cache rows of this thread's keys (pages read one tile ahead)
+        const char* row[NK];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          int64_t page = pg_next[i];
+          if (page < 0 || page >= p.num_pages) {
+            bad = true;
+            page = 0;
+          }
+          const int64_t r = page * p.page_size + key_of(t, i) % p.page_size;
+          row[i] = cache + r * (kFp8 ? mla::kDQK : mla::kDQK * 2);
+        }
+        if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+        load_pages(t + 1);
+        if constexpr (!kFp8) {
+          if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+        }
+        const uint32_t dst = sbase + (kFp8 ? OFF_RAW + (t % NR) * RAW_STAGE : OFF_STAGE + s * STAGE);
+        for (int sl = 0; sl < n_slots; ++sl) {
+          const int dim = sl < 4 ? vdim0 + sl * 64 : 512;
+#pragma unroll
+          for (int i = 0; i < NK; ++i) {
+            const int kk = i * 2 * IPI + lw * IPI + g;
+            if constexpr (kFp8) {
+              ptx::cp_async_16(dst + sl * ATOM8 + kk * 64 + sub * 16, row[i] + dim + sub * 16);
+            } else {
+              ptx::cp_async_16(dst + sl * ATOM + kk * 128 + ((sub ^ (kk & 7)) * 16),
+                               row[i] + (dim + sub * 8) * 2);
+            }
+          }
+        }
+        ptx::cp_async_commit();
+      }
+      if (t == 0) continue;
+      // retire tile u = t - 1
+      const int u = t - 1, su = u % NS;
+      if (t < n_tiles) ptx::cp_async_wait<1>(); else ptx::cp_async_wait<0>();
+      if constexpr (kFp8) {
+        // e4m3 codes -> f16 operands (exact); the per-tensor scale is applied
+        // to the scores and the output instead.
+        if (u >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[su]), ((u / NS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t raw = sbase + OFF_RAW + (u % NR) * RAW_STAGE;
+        const uint32_t dst = sbase + OFF_STAGE + su * STAGE;
+        for (int sl = 0; sl < n_slots; ++sl) {
+#pragma unroll
+          for (int i = 0; i < NK; ++i) {
+            const int kk = i * 2 * IPI + lw * IPI + g;
+            const uint4 codes = ld_shared_u4(raw + sl * ATOM8 + kk * 64 + sub * 16);
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_f16x2(codes.x);
+            lo.y = e4m3x2_to_f16x2(codes.x >> 16);
+            lo.z = e4m3x2_to_f16x2(codes.y);
+            lo.w = e4m3x2_to_f16x2(codes.y >> 16);
+            hi.x = e4m3x2_to_f16x2(codes.z);
+            hi.y = e4m3x2_to_f16x2(codes.z >> 16);
+            hi.z = e4m3x2_to_f16x2(codes.w);
+            hi.w = e4m3x2_to_f16x2(codes.w >> 16);
+            const uint32_t rowp = dst + sl * ATOM + kk * 128;
+            st_shared_u4(rowp + (((2 * sub) ^ (kk & 7)) * 16), lo);
+            st_shared_u4(rowp + (((2 * sub + 1) ^ (kk & 7)) * 16), hi);
+          }
+        }
       }
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_u32(&bars.raw_empty[sr]));
-      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[so]));
+      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[su]));
     }
-    }
+    if (!ok) ptx::cp_async_wait<0>();  // copies in flight land before the CTA winds down
   } else if (warp >= kSoftmaxWarp0) {
     // ----------------------------------------------------------- softmax ---
     const int q4 = warp - kSoftmaxWarp0;       // TMEM lane quarter of this warp
@@ -705,42 +703,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync_all();  // no CTA leaves while its partner may still write into it
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled get_encode() {
-  static EncodeTiled fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(ptr);
-  }
-  return fn;
-}
-
 }  // namespace
 
 int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
-  EncodeTiled encode = get_encode();
-  if (encode == nullptr) return (int)cudaErrorNotSupported;
   const bool fp8 = p.kv_dtype == MLA_KV_FP8_E4M3;
-  CUtensorMap tmap;
-  const cuuint64_t rows_total = (cuuint64_t)p.num_pages * (cuuint64_t)p.page_size;
-  cuuint64_t dims[2] = {(cuuint64_t)mla::kDQK, rows_total};
-  cuuint64_t strides[1] = {(cuuint64_t)mla::kDQK * (fp8 ? 1 : 2)};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&tmap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      2, const_cast<void*>(p.cache), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
   auto kernel = fp8 ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
   const int smem = fp8 ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
   static bool attr_done[2] = {false, false};
@@ -750,6 +716,6 @@ int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
     attr_done[fp8] = true;
   }
   dim3 grid(p.num_splits * 2, p.row_blocks, p.batch);
-  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(tmap, p);
+  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return (int)cudaGetLastError();
 }

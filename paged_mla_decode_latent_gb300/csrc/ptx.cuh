@@ -124,6 +124,22 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// 16-byte global -> shared copy through L2 only (cp.async.cg), in the
+// current commit group of the issuing thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's commit groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
