@@ -9,12 +9,12 @@
 // 64 rope dims).  Each CTA therefore reads only its part of every latent row.
 //
 // Per 64-key tile, in each CTA:
-//   loader warps  : block-table lookup one tile ahead, 16-byte cp.async of
-//                   the tile's rows in 128-byte pieces (one 64-dim slab of one
-//                   key) straight into a 128B-swizzled K-major stage (bf16),
-//                   or into a raw stage that the same threads convert to f16
-//                   (fp8); each thread fences its own copies for the tensor
-//                   cores and arrives on the stage's barrier.
+//   loader warps  : three warps take turns by tile: block-table lookup, then
+//                   16-byte cp.async of the tile's rows in 128-byte pieces
+//                   (one 64-dim slab of one key) straight into a 128B-swizzled
+//                   K-major stage (bf16), or into a raw stage the same lanes
+//                   convert to f16 (fp8); each lane fences its own copies for
+//                   the tensor cores and arrives on the stage's barrier.
 //   MMA warp      : S_part = Q_part K_part^T  (tcgen05, A = Q from TMEM,
 //                   CTA 0's rope part A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
@@ -62,16 +62,16 @@ constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
 constexpr int RECV = 128 * T * 4;      // one partner score tile, fp32
 constexpr int kThreads = 256;
-constexpr int kLoadWarp0 = 2;          // warps 2-3 copy the cache rows
+constexpr int kLoaders = 3;            // loader warps 0, 2, 3: warp (t % 3) copies tile t
 constexpr int kSoftmaxWarp0 = 4;
 
-// Shared-memory plan.  bf16 cache: 3 operand stages the loader warps fill
-// with cp.async.  fp8 cache: 2 raw stages of codes (cp.async) + 2 f16 operand
-// stages the same loader threads convert into.
+// Shared-memory plan.  bf16 cache: 3 operand stages, one per loader warp,
+// filled with cp.async.  fp8 cache: one raw stage of codes per loader warp
+// (cp.async) + 2 f16 operand stages the loader warps convert into.
 template <bool kFp8>
 struct Layout {
   static constexpr int NS = kFp8 ? 2 : 3;   // operand stages (what the MMA reads)
-  static constexpr int NR = kFp8 ? 2 : 0;   // raw fp8 stages
+  static constexpr int NR = kFp8 ? 3 : 0;   // raw fp8 stages (one per loader warp)
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
@@ -94,7 +94,7 @@ constexpr float kMaxSentinel = -1.0e30f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 struct Bars {
-  uint64_t kv_full[3];    // operand stage ready (64 loader threads arrive)
+  uint64_t kv_full[3];    // operand stage ready (the 32 threads of its loader warp arrive)
   uint64_t kv_empty[3];   // operand stage consumed by the MMAs
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -222,7 +222,7 @@ template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(mla::FwdParams p) {
   using L = Layout<kFp8>;
-  constexpr int NS = L::NS, NR = L::NR;
+  constexpr int NS = L::NS;
   constexpr int OFF_STAGE = L::OFF_STAGE, OFF_RAW = L::OFF_RAW, OFF_QROPE = L::OFF_QROPE;
   constexpr int OFF_RECV = L::OFF_RECV, OFF_BAR = L::OFF_BAR;
   constexpr uint32_t kAB = kFp8 ? 0u : 1u;  // operand type: f16 (fp8 cache) or bf16
@@ -268,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 64);
+      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 32);
       ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -366,96 +366,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (warp == kLoadWarp0 || warp == kLoadWarp0 + 1) {
+  } else if (warp == 0 || warp == 2 || warp == 3) {
     // ------------------------------------------------------------ loader ---
-    // Gather of the tile's cache rows with 16-byte cp.async (L2 only).  The
+    // Gather of a tile's cache rows with 16-byte cp.async (L2 only).  The
     // operand layout keeps a key's 64-dim slab contiguous only over 128 B, so
     // every copy is a 128-byte piece of one row: 8 lanes per (key, slab)
-    // piece for bf16 (written straight into the 128B-swizzled stage), 4 lanes
-    // per 64-byte piece of fp8 codes (into a raw stage, converted below by
-    // the thread that copied it).  Thread (warp w, lane l) always serves the
-    // same NK keys of a tile, so it needs NK block-table entries per tile,
-    // read one tile ahead.  Each thread retires tile t-1 after issuing tile
-    // t: waits for its own copies, converts (fp8), fences them for the
-    // tensor cores' async proxy and arrives on the stage's full barrier.
+    // piece for bf16, written straight into the 128B-swizzled stage; 4 lanes
+    // per 64-byte piece of fp8 codes, written into the warp's raw stage and
+    // converted to f16 by the same lanes.  Loader warp w (0, 1, 2 for warps
+    // 0, 2, 3) copies tiles w, w+3, ...: it issues a tile, waits for its own
+    // copies, fences them for the tensor cores' async proxy and arrives on
+    // the stage's full barrier, while the other two warps have their tiles in
+    // flight.  Block-table entries for the warp's next tile are read before
+    // it waits.
     constexpr int LPI = kFp8 ? 4 : 8;        // lanes per piece
     constexpr int IPI = 32 / LPI;            // pieces per warp instruction
-    constexpr int NK = T / (2 * IPI);        // keys per thread: 8 (bf16) or 4 (fp8)
-    const int lw = warp - kLoadWarp0, g = lane / LPI, sub = lane % LPI;
+    constexpr int NK = T / IPI;              // keys per lane: 16 (bf16) or 8 (fp8)
+    const int lw = warp == 0 ? 0 : warp - 1;  // 0, 1, 2
+    const int g = lane / LPI, sub = lane % LPI;
     const int n_slots = rank == 0 ? 5 : 4;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
     const char* cache = static_cast<const char*>(p.cache);
-    auto key_of = [&](int tile, int i) -> int {  // i-th key of this thread, clamped to the split
+    auto key_of = [&](int tile, int i) -> int {  // i-th key of this lane, clamped to the split
       const int start = k0 + tile * T;
-      const int kk = i * 2 * IPI + lw * IPI + g;
-      return start + min(kk, min(T, k1 - start) - 1);
+      return start + min(i * IPI + g, min(T, k1 - start) - 1);
     };
-    int pg_next[NK];
+    int pg[NK];
     auto load_pages = [&](int tile) {
       if (tile >= n_tiles) return;
 #pragma unroll
-      for (int i = 0; i < NK; ++i) pg_next[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
+      for (int i = 0; i < NK; ++i) pg[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
     };
-    load_pages(0);
-    bool ok = true;
-    for (int t = 0; t <= n_tiles; ++t) {
-      if (t < n_tiles) {
-        const int s = t % NS;
-        // cache rows of this thread's keys (pages read one tile ahead)
-        const char* row[NK];
-        bool bad = false;
+    load_pages(lw);
+    for (int t = lw; t < n_tiles; t += kLoaders) {
+      const int s = t % NS;
+      const char* row[NK];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        int64_t page = pg[i];
+        if (page < 0 || page >= p.num_pages) {
+          bad = true;
+          page = 0;
+        }
+        const int64_t r = page * p.page_size + key_of(t, i) % p.page_size;
+        row[i] = cache + r * (kFp8 ? mla::kDQK : mla::kDQK * 2);
+      }
+      if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+      load_pages(t + kLoaders);
+      if constexpr (!kFp8) {
+        if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
+          break;
+      }
+      const uint32_t dst = sbase + (kFp8 ? OFF_RAW + lw * RAW_STAGE : OFF_STAGE + s * STAGE);
+      for (int sl = 0; sl < n_slots; ++sl) {
+        const int dim = sl < 4 ? vdim0 + sl * 64 : 512;
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
-          int64_t page = pg_next[i];
-          if (page < 0 || page >= p.num_pages) {
-            bad = true;
-            page = 0;
-          }
-          const int64_t r = page * p.page_size + key_of(t, i) % p.page_size;
-          row[i] = cache + r * (kFp8 ? mla::kDQK : mla::kDQK * 2);
-        }
-        if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-        load_pages(t + 1);
-        if constexpr (!kFp8) {
-          if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) {
-            ok = false;
-            break;
+          const int kk = i * IPI + g;
+          if constexpr (kFp8) {
+            ptx::cp_async_16(dst + sl * ATOM8 + kk * 64 + sub * 16, row[i] + dim + sub * 16);
+          } else {
+            ptx::cp_async_16(dst + sl * ATOM + kk * 128 + ((sub ^ (kk & 7)) * 16),
+                             row[i] + (dim + sub * 8) * 2);
           }
         }
-        const uint32_t dst = sbase + (kFp8 ? OFF_RAW + (t % NR) * RAW_STAGE : OFF_STAGE + s * STAGE);
-        for (int sl = 0; sl < n_slots; ++sl) {
-          const int dim = sl < 4 ? vdim0 + sl * 64 : 512;
-#pragma unroll
-          for (int i = 0; i < NK; ++i) {
-            const int kk = i * 2 * IPI + lw * IPI + g;
-            if constexpr (kFp8) {
-              ptx::cp_async_16(dst + sl * ATOM8 + kk * 64 + sub * 16, row[i] + dim + sub * 16);
-            } else {
-              ptx::cp_async_16(dst + sl * ATOM + kk * 128 + ((sub ^ (kk & 7)) * 16),
-                               row[i] + (dim + sub * 8) * 2);
-            }
-          }
-        }
-        ptx::cp_async_commit();
       }
-      if (t == 0) continue;
-      // retire tile u = t - 1
-      const int u = t - 1, su = u % NS;
-      if (t < n_tiles) ptx::cp_async_wait<1>(); else ptx::cp_async_wait<0>();
+      ptx::cp_async_commit();
+      ptx::cp_async_wait<0>();
       if constexpr (kFp8) {
         // e4m3 codes -> f16 operands (exact); the per-tensor scale is applied
         // to the scores and the output instead.
-        if (u >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[su]), ((u / NS) - 1) & 1)) {
-          ok = false;
+        if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
           break;
-        }
-        const uint32_t raw = sbase + OFF_RAW + (u % NR) * RAW_STAGE;
-        const uint32_t dst = sbase + OFF_STAGE + su * STAGE;
+        const uint32_t out = sbase + OFF_STAGE + s * STAGE;
         for (int sl = 0; sl < n_slots; ++sl) {
 #pragma unroll
           for (int i = 0; i < NK; ++i) {
-            const int kk = i * 2 * IPI + lw * IPI + g;
-            const uint4 codes = ld_shared_u4(raw + sl * ATOM8 + kk * 64 + sub * 16);
+            const int kk = i * IPI + g;
+            const uint4 codes = ld_shared_u4(dst + sl * ATOM8 + kk * 64 + sub * 16);
             uint4 lo, hi;
             lo.x = e4m3x2_to_f16x2(codes.x);
             lo.y = e4m3x2_to_f16x2(codes.x >> 16);
@@ -465,16 +454,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             hi.y = e4m3x2_to_f16x2(codes.z >> 16);
             hi.z = e4m3x2_to_f16x2(codes.w);
             hi.w = e4m3x2_to_f16x2(codes.w >> 16);
-            const uint32_t rowp = dst + sl * ATOM + kk * 128;
+            const uint32_t rowp = out + sl * ATOM + kk * 128;
             st_shared_u4(rowp + (((2 * sub) ^ (kk & 7)) * 16), lo);
             st_shared_u4(rowp + (((2 * sub + 1) ^ (kk & 7)) * 16), hi);
           }
         }
       }
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[su]));
+      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
     }
-    if (!ok) ptx::cp_async_wait<0>();  // copies in flight land before the CTA winds down
+    ptx::cp_async_wait<0>();  // nothing of this warp is in flight when it leaves
   } else if (warp >= kSoftmaxWarp0) {
     // ----------------------------------------------------------- softmax ---
     const int q4 = warp - kSoftmaxWarp0;       // TMEM lane quarter of this warp
