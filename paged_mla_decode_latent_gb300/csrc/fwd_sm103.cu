@@ -62,16 +62,16 @@ constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
 constexpr int RECV = 128 * T * 4;      // one partner score tile, fp32
 constexpr int kThreads = 256;
-constexpr int kLoaders = 3;            // loader warps 0, 2, 3: warp (t % 3) copies tile t
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxWarp0 = 4;       // warps 4-7; warps 2, 3, 0 load; warp 1 issues MMAs
 
-// Shared-memory plan.  bf16 cache: 3 operand stages, one per loader warp,
-// filled with cp.async.  fp8 cache: one raw stage of codes per loader warp
-// (cp.async) + 2 f16 operand stages the loader warps convert into.
+// Shared-memory plan.  Each operand stage has its own loader warp, so every
+// stage barrier is waited on by one warp, in order.  bf16 cache: 3 operand
+// stages filled with cp.async.  fp8 cache: 2 f16 operand stages, each with a
+// raw stage of codes its loader warp copies into and converts from.
 template <bool kFp8>
 struct Layout {
-  static constexpr int NS = kFp8 ? 2 : 3;   // operand stages (what the MMA reads)
-  static constexpr int NR = kFp8 ? 3 : 0;   // raw fp8 stages (one per loader warp)
+  static constexpr int NS = kFp8 ? 2 : 3;   // operand stages = loader warps
+  static constexpr int NR = kFp8 ? 2 : 0;   // raw fp8 stages (one per loader warp)
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
@@ -102,7 +102,6 @@ struct Bars {
   uint64_t o_done;
   uint64_t q_ready;
   uint64_t drain;
-  uint64_t heavy_bar[2];  // bf16: the four softmax warps' votes are in
   uint32_t tmem_base;
   int32_t abort;
   uint32_t heavy[2];  // bf16: per score buffer, one byte per softmax warp (see the softmax)
@@ -152,6 +151,15 @@ __device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity
 template <bool kCluster>
 __device__ __forceinline__ bool wait_all(const Ctx& c, uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, wait<kCluster>(c, bar, parity));
+}
+
+// 2^x with the SFU's approximate exp2 (inputs below -126 flush to +0, -inf
+// gives +0).  Its relative error is far below the 16-bit rounding the
+// weights get next.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -279,8 +287,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars.heavy_bar[0]), 4);
-    ptx::mbar_init(ptx::smem_u32(&bars.heavy_bar[1]), 4);
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
   }
@@ -366,23 +372,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (warp == 0 || warp == 2 || warp == 3) {
+  } else if (warp == 2 || warp == 3 || (warp == 0 && NS == 3)) {
     // ------------------------------------------------------------ loader ---
     // Gather of a tile's cache rows with 16-byte cp.async (L2 only).  The
     // operand layout keeps a key's 64-dim slab contiguous only over 128 B, so
     // every copy is a 128-byte piece of one row: 8 lanes per (key, slab)
     // piece for bf16, written straight into the 128B-swizzled stage; 4 lanes
     // per 64-byte piece of fp8 codes, written into the warp's raw stage and
-    // converted to f16 by the same lanes.  Loader warp w (0, 1, 2 for warps
-    // 0, 2, 3) copies tiles w, w+3, ...: it issues a tile, waits for its own
-    // copies, fences them for the tensor cores' async proxy and arrives on
-    // the stage's full barrier, while the other two warps have their tiles in
-    // flight.  Block-table entries for the warp's next tile are read before
-    // it waits.
+    // converted to f16 by the same lanes.  Loader warp w (warps 2, 3, 0)
+    // owns operand stage w and copies tiles w, w+NS, ...: it issues a tile,
+    // waits for its own copies, fences them for the tensor cores' async proxy
+    // and arrives on the stage's full barrier, while the other loader warps
+    // have their tiles in flight.  Block-table entries for the warp's next
+    // tile are read before it waits.
     constexpr int LPI = kFp8 ? 4 : 8;        // lanes per piece
     constexpr int IPI = 32 / LPI;            // pieces per warp instruction
     constexpr int NK = T / IPI;              // keys per lane: 16 (bf16) or 8 (fp8)
-    const int lw = warp == 0 ? 0 : warp - 1;  // 0, 1, 2
+    const int lw = warp == 0 ? 2 : warp - 2;  // 0, 1, 2: the operand stage this warp owns
     const int g = lane / LPI, sub = lane % LPI;
     const int n_slots = rank == 0 ? 5 : 4;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
@@ -398,8 +404,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < NK; ++i) pg[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
     };
     load_pages(lw);
-    for (int t = lw; t < n_tiles; t += kLoaders) {
-      const int s = t % NS;
+    for (int t = lw; t < n_tiles; t += NS) {
+      const int s = lw;
       const char* row[NK];
       bool bad = false;
 #pragma unroll
@@ -413,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         row[i] = cache + r * (kFp8 ? mla::kDQK : mla::kDQK * 2);
       }
       if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-      load_pages(t + kLoaders);
+      load_pages(t + NS);
       if constexpr (!kFp8) {
         if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
           break;
@@ -524,15 +530,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       float s[T];
       {
-        uint32_t raw[32];
-        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T, raw);
+        uint32_t raw0[32], raw1[32];
+        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T, raw0);
+        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + 32, raw1);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
-        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + 32, raw);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(raw[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(raw0[i]);
+          s[32 + i] = __uint_as_float(raw1[i]);
+        }
       }
       // Swap partial scores with the partner CTA: asynchronous remote stores
       // that count their bytes on the partner's recv_full barrier, whose
@@ -591,8 +597,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float lsum = 0.f;
 #pragma unroll
       for (int i = 0; i < T / 2; ++i) {
-        float p0 = exp2f(fmaf(s[2 * i], c2, neg_m));
-        float p1 = exp2f(fmaf(s[2 * i + 1], c2, neg_m));
+        float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
+        float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
         if (!full_tile) {
           p0 = 2 * i < lim ? p0 : 0.f;
           p1 = 2 * i + 1 < lim ? p1 : 0.f;
@@ -607,27 +613,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if constexpr (!kFp8) {
         // bf16 keeps 8 significant bits.  Where one key carries a sizeable
         // share of a row's weight (more than 1/64 of the row sum so far), the
-        // rounding would show in O, so the tile also gets a second bf16 term
+        // rounding would show in O, so such rows also get a second bf16 term
         // with what the first rounded away (P = P_hi + P_lo to ~16 bits) and
-        // the MMA warp adds a second PV.  Elsewhere the rounding errors of
-        // many small weights average out.  The decision is per tile for the
-        // whole CTA (one byte per warp, gathered on an mbarrier).
-        const float pmax = lim > 0 ? exp2f(mt - m_run) : 0.f;
+        // the MMA warp adds a second PV for the tile.  Elsewhere the rounding
+        // errors of many small weights average out.  Each warp votes with one
+        // byte; warps that vote no write zeros as their second term, so the
+        // second PV is right for every row whichever warps voted.
+        const float pmax = lim > 0 ? fast_exp2(mt - m_run) : 0.f;
         const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
-        if (lane == 0) {
-          reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
-          ptx::mbar_arrive(ptx::smem_u32(&bars.heavy_bar[buf]));
-        }
-        if (!wait_all<false>(c, ptx::smem_u32(&bars.heavy_bar[buf]), (t >> 1) & 1)) { ok = false; break; }
-        if (*reinterpret_cast<volatile uint32_t*>(&bars.heavy[buf]) != 0) {
-          uint32_t pl[32];
+        uint32_t pl[32];
+        if (heavy) {  // warp-uniform
 #pragma unroll
           for (int i = 0; i < T / 2; ++i) {
             const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
             pl[i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
           }
-          ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
+        } else {
+#pragma unroll
+          for (int i = 0; i < T / 2; ++i) pl[i] = 0u;
         }
+        ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
+        if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
