@@ -162,6 +162,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe: x = n + f with n = floor(x), f in [0, 1); 2^f from a
+// degree-4 polynomial fitted (least squares in relative error on Chebyshev
+// nodes of [0, 1]) to within 2.7e-6 relative; n goes into the exponent bits.
+// Half of the weights take this path so the SFU and the FMA pipe share the
+// exponentials.  Inputs below -127 give +0.
+__device__ __forceinline__ float poly_exp2(float x) {
+  x = fmaxf(x, -127.f);
+  const float n = floorf(x);
+  const float f = x - n;
+  float p = fmaf(0.013520603f, f, 0.052037429f);
+  p = fmaf(p, f, 0.24142750f);
+  p = fmaf(p, f, 0.69300663f);
+  p = fmaf(p, f, 1.0000025f);
+  return __int_as_float(__float_as_int(p) + (__float2int_rn(n) << 23));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -563,10 +579,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // last tile of a split and causal rows need the mask.
       const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
       const bool full_tile = lim >= T;
-      float mt_raw = -INFINITY;
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < T; ++i)
-        if (full_tile || i < lim) mt_raw = fmaxf(mt_raw, s[i]);
+        if (full_tile || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt = lim > 0 ? mt_raw * c2 : -INFINITY;
       const bool need = mt > m_run + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -593,24 +613,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Weights p = 2^(s*c2 - m) (s now holds them), written as 16-bit pairs
       // over the consumed score columns.  The row sum is exact (fp32).
       const float neg_m = -m_run;
-      uint32_t pk[32];
-      float lsum = 0.f;
+      uint32_t pk[64];  // [0, 32): weights; [32, 64): bf16 second-order terms
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < T / 2; ++i) {
         float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
-        float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
+        float p1 = poly_exp2(fmaf(s[2 * i + 1], c2, neg_m));
         if (!full_tile) {
           p0 = 2 * i < lim ? p0 : 0.f;
           p1 = 2 * i + 1 < lim ? p1 : 0.f;
         }
         s[2 * i] = p0;
         s[2 * i + 1] = p1;
-        lsum += p0 + p1;
+        ls[i & 3] += p0 + p1;
         pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
       }
-      l_run += lsum;
-      ptx::tmem_st32(tmem + lanes + TM_S + buf * T, pk);
-      if constexpr (!kFp8) {
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      if constexpr (kFp8) {
+        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      } else {
         // bf16 keeps 8 significant bits.  Where one key carries a sizeable
         // share of a row's weight (more than 1/64 of the row sum so far), the
         // rounding would show in O, so such rows also get a second bf16 term
@@ -621,18 +642,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // second PV is right for every row whichever warps voted.
         const float pmax = lim > 0 ? fast_exp2(mt - m_run) : 0.f;
         const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
-        uint32_t pl[32];
         if (heavy) {  // warp-uniform
 #pragma unroll
           for (int i = 0; i < T / 2; ++i) {
             const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-            pl[i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
+            pk[32 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < T / 2; ++i) pl[i] = 0u;
+          for (int i = 0; i < T / 2; ++i) pk[32 + i] = 0u;
         }
-        ptx::tmem_st32(tmem + lanes + TM_S + buf * T + 32, pl);
+        ptx::tmem_st64(tmem + lanes + TM_S + buf * T, pk);
         if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
       }
       ptx::tmem_st_wait();
