@@ -162,22 +162,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe: x = n + f with n = floor(x), f in [0, 1); 2^f from a
-// degree-4 polynomial fitted (least squares in relative error on Chebyshev
-// nodes of [0, 1]) to within 2.7e-6 relative; n goes into the exponent bits.
-// Half of the weights take this path so the SFU and the FMA pipe share the
-// exponentials.  Inputs below -127 give +0.
-__device__ __forceinline__ float poly_exp2(float x) {
-  x = fmaxf(x, -127.f);
-  const float n = floorf(x);
-  const float f = x - n;
-  float p = fmaf(0.013520603f, f, 0.052037429f);
-  p = fmaf(p, f, 0.24142750f);
-  p = fmaf(p, f, 0.69300663f);
-  p = fmaf(p, f, 1.0000025f);
-  return __int_as_float(__float_as_int(p) + (__float2int_rn(n) << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -618,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < T / 2; ++i) {
         float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
-        float p1 = poly_exp2(fmaf(s[2 * i + 1], c2, neg_m));
+        float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
         if (!full_tile) {
           p0 = 2 * i < lim ? p0 : 0.f;
           p1 = 2 * i + 1 < lim ? p1 : 0.f;
