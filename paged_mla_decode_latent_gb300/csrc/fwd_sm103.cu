@@ -60,7 +60,14 @@ constexpr int SLOTS = 5;               // slabs per stage (CTA 0: 4 value + 1 ro
 constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
-constexpr int RECV = 128 * T * 4;      // one partner score tile, fp32
+// Exchange with the partner CTA.  Each CTA owns the softmax of 64 of the 128
+// rows; it receives the partner's partial scores of those rows and returns
+// their weights.
+constexpr int RECV_S = 64 * T * 4;     // partner's partial scores of my 64 rows (16 KB)
+constexpr int RP_HI = 0, RP_LO = 32 * 128, RP_ALPHA = 2 * 32 * 128, RP_HDR = RP_ALPHA + 32 * 4;
+constexpr int RECV_P = RP_HDR + 256;   // one partner warp's weights for my 32 rows + header
+constexpr int RECV_FIN = 32 * 4;       // 1/l of 32 rows
+constexpr int XCHG = 2 * RECV_S + 4 * RECV_P + 2 * RECV_FIN;
 constexpr int kThreads = 256;
 constexpr int kSoftmaxWarp0 = 4;       // warps 4-7; warps 2, 3, 0 load; warp 1 issues MMAs
 
@@ -76,7 +83,7 @@ struct Layout {
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
   static constexpr int OFF_RECV = OFF_QROPE + QROPE;
-  static constexpr int OFF_BAR = OFF_RECV + 2 * RECV;
+  static constexpr int OFF_BAR = OFF_RECV + XCHG;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 };
 static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
@@ -98,7 +105,10 @@ struct Bars {
   uint64_t kv_empty[3];   // operand stage consumed by the MMAs
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t recv_full[2];
+  uint64_t recv_full[2];      // partner's partial scores of my rows landed (16 KB)
+  uint64_t recvp_full[2][2];  // [buf][pair]: partner warp's weights + header landed
+  uint64_t recvlo_full[2][2]; // [buf][pair]: partner warp's low-order weights landed
+  uint64_t fin_full[2];       // [pair]: partner warp's 1/l landed
   uint64_t o_done;
   uint64_t q_ready;
   uint64_t drain;
@@ -185,6 +195,12 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr)
                : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
 
@@ -283,6 +299,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 128);
       ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i]), 1);
+      for (int j = 0; j < 2; ++j) {
+        ptx::mbar_init(ptx::smem_u32(&bars.recvp_full[i][j]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars.recvlo_full[i][j]), 1);
+      }
+      ptx::mbar_init(ptx::smem_u32(&bars.fin_full[i]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
@@ -520,9 +541,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
+    // Row split.  This CTA owns the softmax of rows [64 rank, 64 rank + 64),
+    // which sit in its TMEM lane quarters 2 rank and 2 rank + 1 (the "owner"
+    // warps).  Its other two softmax warps ("helpers") hold the partner's
+    // rows: each tile they send the partner their partial scores of those
+    // rows and take back the weights (and the rescale factors) to write into
+    // this CTA's TMEM.  Owner warp (quarter q) of one CTA and helper warp
+    // (quarter q) of the other serve the same 32 rows.
+    const bool owner = (q4 >> 1) == (int)rank;
+    const int pair = q4 & 1;             // which of the two owner (or helper) warps
+    const int orow = pair * 32 + lane;   // row within a CTA's 64-row share
+    const uint32_t x_s = sbase + OFF_RECV;            // [2] partner partial scores of my rows
+    const uint32_t x_p = x_s + 2 * RECV_S;            // [2][2] partner weights for my helper rows
+    const uint32_t x_fin = x_p + 4 * RECV_P;          // [2] partner 1/l for my helper rows
+    const uint32_t peer_x = ptx::mapa(x_s, peer);
+    constexpr uint32_t kPBytes = 32 * 128 + 32 * 4 + 16;  // weights + factors + header
     float m_run = kMaxSentinel, l_run = 0.f;
-    const uint32_t recv_local = sbase + OFF_RECV;
-    const uint32_t recv_peer = ptx::mapa(recv_local, peer);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
@@ -540,115 +574,179 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[32 + i] = __uint_as_float(raw1[i]);
         }
       }
-      // Swap partial scores with the partner CTA: asynchronous remote stores
-      // that count their bytes on the partner's recv_full barrier, whose
-      // arrival is this CTA's own expect_tx of the 32 KB it will receive.
-      const uint32_t my_off = (uint32_t)(buf * RECV + r * 16);
-      const uint32_t peer_bar = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer);
-#pragma unroll
-      for (int q = 0; q < T / 4; ++q)
-        ptx::st_async_v4(recv_peer + my_off + q * 128 * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
-                         s[4 * q + 3], peer_bar);
-      if (r == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars.recv_full[buf]), RECV);
-      if (!wait_all<false>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
-#pragma unroll
-      for (int q = 0; q < T / 4; ++q) {
-        float4 v = ld_shared_v4(recv_local + my_off + q * 128 * 16);
-        s[4 * q] += v.x;
-        s[4 * q + 1] += v.y;
-        s[4 * q + 2] += v.z;
-        s[4 * q + 3] += v.w;
-      }
-      // Row max over the visible keys of this tile (log2 domain).  Only the
-      // last tile of a split and causal rows need the mask.
-      const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
-      const bool full_tile = lim >= T;
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < T; ++i)
-        if (full_tile || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-      const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mt = lim > 0 ? mt_raw * c2 : -INFINITY;
-      const bool need = mt > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? fmaxf(m_run, mt) : m_run;
-        const float alpha = exp2f(m_run - m_new);
-        if (t > 0) {
-          // O must not be touched while PV(t-1) is still accumulating
-          if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            ptx::tmem_st32(tmem + lanes + TM_O + ch * 32, o);
-          }
-          ptx::tmem_st_wait();
-        }
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      // Weights p = 2^(s*c2 - m) (s now holds them), written as 16-bit pairs
-      // over the consumed score columns.  The row sum is exact (fp32).
-      const float neg_m = -m_run;
+      const uint32_t p_off = (uint32_t)((buf * 2 + pair) * RECV_P);
       uint32_t pk[64];  // [0, 32): weights; [32, 64): bf16 second-order terms
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      bool heavy = false;
+      float alpha = 1.f;
+      if (owner) {
+        // ---- owner: partner's partial scores of my rows, then the softmax
+        if (pair == 0 && lane == 0)
+          ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars.recv_full[buf]), RECV_S);
+        if (!wait_all<false>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
 #pragma unroll
-      for (int i = 0; i < T / 2; ++i) {
-        float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
-        float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
-        if (!full_tile) {
-          p0 = 2 * i < lim ? p0 : 0.f;
-          p1 = 2 * i + 1 < lim ? p1 : 0.f;
+        for (int q = 0; q < T / 4; ++q) {
+          const float4 v = ld_shared_v4(x_s + buf * RECV_S + (q * 64 + orow) * 16);
+          s[4 * q] += v.x;
+          s[4 * q + 1] += v.y;
+          s[4 * q + 2] += v.z;
+          s[4 * q + 3] += v.w;
         }
-        s[2 * i] = p0;
-        s[2 * i + 1] = p1;
-        ls[i & 3] += p0 + p1;
-        pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
-      }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if constexpr (kFp8) {
-        ptx::tmem_st32(tmem + lanes + TM_S + buf * T, *reinterpret_cast<uint32_t(*)[32]>(pk));
-      } else {
-        // bf16 keeps 8 significant bits.  Where one key carries a sizeable
-        // share of a row's weight (more than 1/64 of the row sum so far), the
-        // rounding would show in O, so such rows also get a second bf16 term
-        // with what the first rounded away (P = P_hi + P_lo to ~16 bits) and
-        // the MMA warp adds a second PV for the tile.  Elsewhere the rounding
-        // errors of many small weights average out.  Each warp votes with one
-        // byte; warps that vote no write zeros as their second term, so the
-        // second PV is right for every row whichever warps voted.
-        const float pmax = lim > 0 ? fast_exp2(mt - m_run) : 0.f;
-        const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
-        if (heavy) {  // warp-uniform
+        // Row max over the visible keys of this tile (log2 domain).  Only the
+        // last tile of a split and causal rows need the mask.
+        const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
+        const bool full_tile = lim >= T;
+        float mx[8];
 #pragma unroll
-          for (int i = 0; i < T / 2; ++i) {
-            const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-            pk[32 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
+        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < T; ++i)
+          if (full_tile || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = lim > 0 ? mt_raw * c2 : -INFINITY;
+        const bool need = mt > m_run + kRescaleThreshold;
+        if (need) {
+          const float m_new = fmaxf(m_run, mt);
+          alpha = exp2f(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        // Weights p = 2^(s*c2 - m) (s now holds them).  The row sum is exact.
+        const float neg_m = -m_run;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < T / 2; ++i) {
+          float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
+          float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
+          if (!full_tile) {
+            p0 = 2 * i < lim ? p0 : 0.f;
+            p1 = 2 * i + 1 < lim ? p1 : 0.f;
           }
-        } else {
+          s[2 * i] = p0;
+          s[2 * i + 1] = p1;
+          ls[i & 3] += p0 + p1;
+          pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+        }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if constexpr (!kFp8) {
+          // bf16 keeps 8 significant bits.  Where one key carries a sizeable
+          // share of a row's weight (more than 1/64 of the row sum so far),
+          // the rounding would show in O, so the warp's rows also get a
+          // second bf16 term with what the first rounded away (P = P_hi + P_lo
+          // to ~16 bits) and the MMA warp adds a second PV for the tile.
+          // Elsewhere the rounding errors of many small weights average out.
+          const float pmax = lim > 0 ? fast_exp2(mt - m_run) : 0.f;
+          heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
+          if (heavy) {  // warp-uniform
+#pragma unroll
+            for (int i = 0; i < T / 2; ++i) {
+              const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
+              pk[32 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
+            }
+          }
+        }
+        if (!heavy) {
 #pragma unroll
           for (int i = 0; i < T / 2; ++i) pk[32 + i] = 0u;
         }
-        ptx::tmem_st64(tmem + lanes + TM_S + buf * T, pk);
-        if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
+        // Weights, rescale factor and (lane 0) a header to the partner's
+        // helper warp for these rows; the low-order terms only when heavy.
+        const uint32_t dst = peer_x + 2 * RECV_S + p_off;
+        const uint32_t bar_p = ptx::mapa(ptx::smem_u32(&bars.recvp_full[buf][pair]), peer);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          ptx::st_async_u4(dst + RP_HI + (q * 32 + lane) * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                           pk[4 * q + 3], bar_p);
+        ptx::st_async_b32(dst + RP_ALPHA + lane * 4, __float_as_uint(alpha), bar_p);
+        if (lane == 0) ptx::st_async_u4(dst + RP_HDR, heavy ? 1u : 0u, 0u, 0u, 0u, bar_p);
+        if (heavy) {
+          const uint32_t bar_lo = ptx::mapa(ptx::smem_u32(&bars.recvlo_full[buf][pair]), peer);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            ptx::st_async_u4(dst + RP_LO + (q * 32 + lane) * 16, pk[32 + 4 * q], pk[33 + 4 * q],
+                             pk[34 + 4 * q], pk[35 + 4 * q], bar_lo);
+        }
+      } else {
+        // ---- helper: my partial scores of the partner's rows go out ...
+        const uint32_t dst = peer_x + buf * RECV_S;
+        const uint32_t bar_s = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer);
+#pragma unroll
+        for (int q = 0; q < T / 4; ++q)
+          ptx::st_async_v4(dst + (q * 64 + orow) * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
+                           s[4 * q + 3], bar_s);
+        // ... and their weights come back
+        const uint32_t rp = ptx::smem_u32(&bars.recvp_full[buf][pair]);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(rp, kPBytes);
+        if (!wait_all<false>(c, rp, (t >> 1) & 1)) { ok = false; break; }
+        const uint32_t src = x_p + p_off;
+        heavy = ld_shared_u4(src + RP_HDR).x != 0;
+        alpha = __uint_as_float(ld_shared_u32(src + RP_ALPHA + lane * 4));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = ld_shared_u4(src + RP_HI + (q * 32 + lane) * 16);
+          pk[4 * q] = v.x;
+          pk[4 * q + 1] = v.y;
+          pk[4 * q + 2] = v.z;
+          pk[4 * q + 3] = v.w;
+        }
+        const uint32_t rlo = ptx::smem_u32(&bars.recvlo_full[buf][pair]);
+        if (heavy) {  // warp-uniform
+          if (lane == 0) ptx::mbar_arrive_expect_tx(rlo, 32 * 128);
+          if (!wait_all<false>(c, rlo, (t >> 1) & 1)) { ok = false; break; }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = ld_shared_u4(src + RP_LO + (q * 32 + lane) * 16);
+            pk[32 + 4 * q] = v.x;
+            pk[33 + 4 * q] = v.y;
+            pk[34 + 4 * q] = v.z;
+            pk[35 + 4 * q] = v.w;
+          }
+        } else {
+          if (lane == 0) ptx::mbar_arrive(rlo);  // no low-order terms this tile
+#pragma unroll
+          for (int i = 0; i < T / 2; ++i) pk[32 + i] = 0u;
+        }
       }
+      // Rescale this CTA's half of O for these rows (the PV of the previous
+      // tile must have finished accumulating).
+      if (__any_sync(0xffffffffu, alpha != 1.f) && t > 0) {
+        if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st32(tmem + lanes + TM_O + ch * 32, o);
+        }
+      }
+      ptx::tmem_st64(tmem + lanes + TM_S + buf * T, pk);
+      if (!kFp8 && lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
     }
 
     // ---------------------------------------------------------- epilogue ---
+    // Owners know 1/l of their rows and send it to the partner's helpers.
+    float inv = 0.f;
+    if (ok) {
+      if (owner) {
+        inv = l_run > 0.f ? s_kv / l_run : 0.f;
+        ptx::st_async_b32(peer_x + 2 * RECV_S + 4 * RECV_P + pair * RECV_FIN + lane * 4,
+                          __float_as_uint(inv),
+                          ptx::mapa(ptx::smem_u32(&bars.fin_full[pair]), peer));
+      } else {
+        const uint32_t fb = ptx::smem_u32(&bars.fin_full[pair]);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, RECV_FIN);
+        ok = wait_all<false>(c, fb, 0);
+        if (ok) inv = __uint_as_float(ld_shared_u32(x_fin + pair * RECV_FIN + lane * 4));
+      }
+    }
     if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
       ptx::tc_fence_after();
-      const float inv = l_run > 0.f ? s_kv / l_run : 0.f;
-      const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       const bool single = p.num_splits == 1;
       uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
       const size_t prow = ((size_t)b * p.num_splits + split) * p.rows + row;
@@ -677,7 +775,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (valid_row && rank == 0) {
+      if (valid_row && owner) {
+        const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
         if (single) p.lse[(size_t)b * p.rows + row] = lse;
         else p.part_lse[prow] = lse;
       }
