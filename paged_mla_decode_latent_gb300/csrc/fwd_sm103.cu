@@ -19,12 +19,18 @@
 //                   CTA 0's rope part A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
 //                   stage read MN-major as V).
-//   softmax warps : read S_part from TMEM, swap it with the partner CTA over
-//                   distributed shared memory (st.async counted on the
-//                   partner's mbarrier), add (identical order in both CTAs,
-//                   so both see bit-identical scores), mask, online softmax
-//                   with a lazily rescaled running max, P -> TMEM over the
-//                   consumed score columns (bf16 as a high + low pair).
+//   softmax warps : eight warps, two per TMEM lane quarter; of each tile the
+//                   first reads keys 0..31 of its 32 rows, the second keys
+//                   32..63.  Each sends its block of partial scores to the
+//                   same warp of the partner CTA over distributed shared
+//                   memory (st.async counted on the partner's mbarrier),
+//                   adds the partner's block (a + b in one CTA, b + a in the
+//                   other: bit-identical sums), swaps its row maxima with
+//                   its sibling warp, then runs the online softmax with a
+//                   lazily rescaled running max and writes its weights to
+//                   TMEM over the consumed score columns (bf16: a high part
+//                   and, on tiles where one key carries much of a row's
+//                   weight, a low part).
 // The epilogue normalises O and writes bf16 output (one split) or fp32
 // partials plus the per-row log-sum-exp (several splits).
 //
@@ -60,16 +66,17 @@ constexpr int SLOTS = 5;               // slabs per stage (CTA 0: 4 value + 1 ro
 constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
-// Exchange with the partner CTA.  Each CTA owns the softmax of 64 of the 128
-// rows; it receives the partner's partial scores of those rows and returns
-// their weights.
-constexpr int RECV_S = 64 * T * 4;     // partner's partial scores of my 64 rows (16 KB)
-constexpr int RP_HI = 0, RP_LO = 32 * 128, RP_ALPHA = 2 * 32 * 128, RP_HDR = RP_ALPHA + 32 * 4;
-constexpr int RECV_P = RP_HDR + 256;   // one partner warp's weights for my 32 rows + header
-constexpr int RECV_FIN = 32 * 4;       // 1/l of 32 rows
-constexpr int XCHG = 2 * RECV_S + 4 * RECV_P + 2 * RECV_FIN;
-constexpr int kThreads = 256;
-constexpr int kSoftmaxWarp0 = 4;       // warps 4-7; warps 2, 3, 0 load; warp 1 issues MMAs
+// Exchange with the partner CTA: each softmax warp sends and receives one
+// 32-row x 32-key block of fp32 partial scores per tile.
+constexpr int kSoftmaxWarps = 8;
+constexpr int RECV_W = 32 * 32 * 4;                  // one warp's block (4 KB)
+constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (32 KB)
+constexpr int X_FREE = 2 * RECV;                     // [2][8] words the "buffer free" signals land in
+constexpr int X_MAX = X_FREE + 128;                  // [2 bufs][2 key halves][128 rows] row maxima
+constexpr int X_L = X_MAX + 2 * 2 * 128 * 4;         // [2 key halves][128 rows] row sums
+constexpr int XCHG = X_L + 2 * 128 * 4;
+constexpr int kThreads = 128 + 32 * kSoftmaxWarps;  // 12 warps
+constexpr int kSoftmaxWarp0 = 4;       // warps 4-11; warps 2, 3, 0 load; warp 1 issues MMAs
 
 // Shared-memory plan.  Each operand stage has its own loader warp, so every
 // stage barrier is waited on by one warp, in order.  bf16 cache: 3 operand
@@ -84,7 +91,7 @@ struct Layout {
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
   static constexpr int OFF_RECV = OFF_QROPE + QROPE;
   static constexpr int OFF_BAR = OFF_RECV + XCHG;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers + alignment slack
 };
 static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
 static_assert(Layout<true>::SMEM_BYTES <= 232448, "fp8 smem");
@@ -105,18 +112,18 @@ struct Bars {
   uint64_t kv_empty[3];   // operand stage consumed by the MMAs
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t recv_full[2];      // partner's partial scores of my rows landed (16 KB)
-  uint64_t recvp_full[2][2];  // [buf][pair]: partner warp's weights + header landed
-  uint64_t recvlo_full[2][2]; // [buf][pair]: partner warp's low-order weights landed
-  uint64_t fin_full[2];       // [pair]: partner warp's 1/l landed
+  uint64_t recv_full[2][kSoftmaxWarps];  // the partner warp's partial scores landed (4 KB)
+  uint64_t recv_free[2][kSoftmaxWarps];  // the partner warp has read what this warp sent
+  uint64_t xm_full[2][4];                // both sibling warps of a lane quarter wrote their maxima
+  uint64_t xl_full[4];                   // both sibling warps wrote their row sums
   uint64_t o_done;
   uint64_t q_ready;
   uint64_t drain;
   uint32_t tmem_base;
   int32_t abort;
-  uint32_t heavy[2];  // bf16: per score buffer, one byte per softmax warp (see the softmax)
+  uint64_t heavy[2];  // bf16: per score buffer, one byte per softmax warp (see the softmax)
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct Ctx {
   int32_t* status;
@@ -198,16 +205,20 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
@@ -297,16 +308,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 128);
-      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i]), 1);
-      for (int j = 0; j < 2; ++j) {
-        ptx::mbar_init(ptx::smem_u32(&bars.recvp_full[i][j]), 1);
-        ptx::mbar_init(ptx::smem_u32(&bars.recvlo_full[i][j]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * kSoftmaxWarps);
+      for (int w = 0; w < kSoftmaxWarps; ++w) {
+        ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i][w]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars.recv_free[i][w]), 1);
       }
-      ptx::mbar_init(ptx::smem_u32(&bars.fin_full[i]), 1);
+      for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xm_full[i][q]), 64);
     }
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xl_full[q]), 64);
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 128);
+    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * kSoftmaxWarps);
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
@@ -372,7 +383,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1)) {
           ptx::tc_fence_after();
-          const bool second = *reinterpret_cast<volatile uint32_t*>(&bars.heavy[np & 1]) != 0;
+          const bool second = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[np & 1]) != 0;
           issue_pv(np++, second);
           progress = true;
         }
@@ -493,7 +504,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cp_async_wait<0>();  // nothing of this warp is in flight when it leaves
   } else if (warp >= kSoftmaxWarp0) {
     // ----------------------------------------------------------- softmax ---
-    const int q4 = warp - kSoftmaxWarp0;       // TMEM lane quarter of this warp
+    // Softmax warp sw (0..7) reads TMEM lane quarter q4 = warp % 4 (rows
+    // 32 q4 .. 32 q4 + 31 of the block) and owns key half g = sw / 4 of every
+    // tile.  The two warps of a quarter ("siblings") keep the same running
+    // max for their rows (they swap tile maxima) and separate row sums.
+    const int sw = warp - kSoftmaxWarp0;
+    const int q4 = warp & 3;                   // TMEM lane quarter of this warp
+    const int g = sw >> 2;                     // key half: keys 32g .. 32g + 31 of a tile
     const int r = q4 * 32 + lane;              // row within the 128-row block
     const int row = rb * mla::kRowTile + r;    // row within the sequence
     const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
@@ -506,13 +523,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const int lim_all = min(nvis, k1);  // keys [k0, lim_all) are visible in this split
 
-    // Q (this CTA's 256 latent dims) -> TMEM as bf16 pairs; CTA 0 also puts
-    // the 64 rope dims into shared memory (128B-swizzled K-major).
+    // Q (this CTA's 256 latent dims) -> TMEM as 16-bit pairs, two 64-dim
+    // chunks per sibling; on CTA 0 the second sibling also puts the 64 rope
+    // dims into shared memory (128B-swizzled K-major).
     {
       const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.rows + row) * mla::kDQK);
       uint32_t buf[32];
       bool q_range = false;
-      for (int chunk = 0; chunk < 4; ++chunk) {
+      for (int chunk = 2 * g; chunk < 2 * g + 2; ++chunk) {
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           uint4 x = valid_row ? qv[(vdim0 + chunk * 64) / 8 + v] : make_uint4(0, 0, 0, 0);
@@ -524,7 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::tmem_st32(tmem + lanes + TM_Q + chunk * 32, buf);
       }
-      if (rank == 0) {
+      if (rank == 0 && g == 1) {
         uint8_t* qr = smem + OFF_QROPE + r * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -541,84 +559,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
-    // Row split.  This CTA owns the softmax of rows [64 rank, 64 rank + 64),
-    // which sit in its TMEM lane quarters 2 rank and 2 rank + 1 (the "owner"
-    // warps).  Its other two softmax warps ("helpers") hold the partner's
-    // rows: each tile they send the partner their partial scores of those
-    // rows and take back the weights (and the rescale factors) to write into
-    // this CTA's TMEM.  Owner warp (quarter q) of one CTA and helper warp
-    // (quarter q) of the other serve the same 32 rows.
-    const bool owner = (q4 >> 1) == (int)rank;
-    const int pair = q4 & 1;             // which of the two owner (or helper) warps
-    const int orow = pair * 32 + lane;   // row within a CTA's 64-row share
-    const uint32_t x_s = sbase + OFF_RECV;            // [2] partner partial scores of my rows
-    const uint32_t x_p = x_s + 2 * RECV_S;            // [2][2] partner weights for my helper rows
-    const uint32_t x_fin = x_p + 4 * RECV_P;          // [2] partner 1/l for my helper rows
-    const uint32_t peer_x = ptx::mapa(x_s, peer);
-    constexpr uint32_t kPBytes = 32 * 128 + 32 * 4 + 16;  // weights + factors + header
-    float m_run = kMaxSentinel, l_run = 0.f;
+    float m_run = kMaxSentinel;  // running max (log2 domain), the same in both siblings
+    float l_run = 0.f;           // exact row sum over this warp's keys only
+    const uint32_t my_recv = sbase + OFF_RECV + sw * RECV_W;  // + buf * RECV
+    const uint32_t peer_recv = ptx::mapa(my_recv, peer);
+    const uint32_t peer_free = ptx::mapa(sbase + OFF_RECV + X_FREE + sw * 4, peer);  // + buf * 32
+    const uint32_t x_max = sbase + OFF_RECV + X_MAX;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       if (!wait_all<false>(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
       ptx::tc_fence_after();
-      float s[T];
+      float s[32];
       {
-        uint32_t raw0[32], raw1[32];
-        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T, raw0);
-        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + 32, raw1);
+        uint32_t raw[32];
+        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + g * 32, raw);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(raw0[i]);
-          s[32 + i] = __uint_as_float(raw1[i]);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
+      }
+      // Swap partial-score blocks with the same warp of the partner CTA.  The
+      // block of tile t goes into the partner's buffer t % 2 once the partner
+      // has read what this warp put there for tile t - 2.
+      if (t >= 2) {
+        const uint32_t fb = ptx::smem_u32(&bars.recv_free[buf][sw]);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, 4);
+        if (!wait_all<false>(c, fb, ((t >> 1) - 1) & 1)) { ok = false; break; }
+      }
+      {
+        const uint32_t dst = peer_recv + buf * RECV + lane * 16;
+        const uint32_t bar = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf][sw]), peer);
+#pragma unroll
+        for (int qd = 0; qd < 8; ++qd)
+          ptx::st_async_v4(dst + qd * 512, s[4 * qd], s[4 * qd + 1], s[4 * qd + 2], s[4 * qd + 3], bar);
+      }
+      {
+        const uint32_t rf = ptx::smem_u32(&bars.recv_full[buf][sw]);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(rf, RECV_W);
+        if (!wait_all<false>(c, rf, (t >> 1) & 1)) { ok = false; break; }
+        const uint32_t src = my_recv + buf * RECV + lane * 16;
+#pragma unroll
+        for (int qd = 0; qd < 8; ++qd) {
+          const float4 v = ld_shared_v4(src + qd * 512);
+          s[4 * qd] += v.x;
+          s[4 * qd + 1] += v.y;
+          s[4 * qd + 2] += v.z;
+          s[4 * qd + 3] += v.w;
         }
       }
-      const uint32_t p_off = (uint32_t)((buf * 2 + pair) * RECV_P);
-      uint32_t pk[64];  // [0, 32): weights; [32, 64): bf16 second-order terms
-      bool heavy = false;
-      float alpha = 1.f;
-      if (owner) {
-        // ---- owner: partner's partial scores of my rows, then the softmax
-        if (pair == 0 && lane == 0)
-          ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars.recv_full[buf]), RECV_S);
-        if (!wait_all<false>(c, ptx::smem_u32(&bars.recv_full[buf]), (t >> 1) & 1)) { ok = false; break; }
-#pragma unroll
-        for (int q = 0; q < T / 4; ++q) {
-          const float4 v = ld_shared_v4(x_s + buf * RECV_S + (q * 64 + orow) * 16);
-          s[4 * q] += v.x;
-          s[4 * q + 1] += v.y;
-          s[4 * q + 2] += v.z;
-          s[4 * q + 3] += v.w;
-        }
-        // Row max over the visible keys of this tile (log2 domain).  Only the
-        // last tile of a split and causal rows need the mask.
-        const int lim = lim_all - (k0 + t * T);  // visible keys of this tile for this row
-        const bool full_tile = lim >= T;
+      // Row max over this warp's visible keys, then over both halves of the
+      // tile (swapped with the sibling warp).  Only the last tile of a split
+      // and causal rows need the mask.
+      const int lim_row = lim_all - (k0 + t * T);  // visible keys of this tile for this row
+      const int lim = lim_row - g * 32;            // ... among this warp's 32 keys
+      const bool full = lim >= 32;
+      float my_mx;
+      {
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < T; ++i)
-          if (full_tile || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float mt = lim > 0 ? mt_raw * c2 : -INFINITY;
-        const bool need = mt > m_run + kRescaleThreshold;
-        if (need) {
-          const float m_new = fmaxf(m_run, mt);
-          alpha = exp2f(m_run - m_new);
-          l_run *= alpha;
-          m_run = m_new;
+        for (int i = 0; i < 32; ++i)
+          if (full || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        my_mx = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      }
+      float sib_mx;
+      {
+        st_shared_f32(x_max + ((buf * 2 + g) * 128 + r) * 4, my_mx);
+        const uint32_t xb = ptx::smem_u32(&bars.xm_full[buf][q4]);
+        ptx::mbar_arrive(xb);
+        if (!wait_all<false>(c, xb, (t >> 1) & 1)) { ok = false; break; }
+        sib_mx = ld_shared_f32(x_max + ((buf * 2 + (g ^ 1)) * 128 + r) * 4);
+      }
+      const float mt = lim_row > 0 ? fmaxf(my_mx, sib_mx) * c2 : -INFINITY;
+      const bool need = mt > m_run + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {  // the same decision in both siblings
+        const float m_new = need ? fmaxf(m_run, mt) : m_run;
+        const float alpha = exp2f(m_run - m_new);
+        if (t > 0) {
+          // This warp's half of the CTA's O columns; the PV of the previous
+          // tile must have finished accumulating.
+          if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o[32];
+            const uint32_t col = tmem + lanes + TM_O + g * 128 + ch * 32;
+            ptx::tmem_ld32(col, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(col, o);
+          }
         }
-        // Weights p = 2^(s*c2 - m) (s now holds them).  The row sum is exact.
-        const float neg_m = -m_run;
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      // Weights p = 2^(s*c2 - m) (s now holds them); the row sum is exact.
+      const float neg_m = -m_run;
+      uint32_t pk[32];  // [0, 16): weights as 16-bit pairs; [16, 32): bf16 low-order terms
+      {
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < T / 2; ++i) {
+        for (int i = 0; i < 16; ++i) {
           float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
           float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
-          if (!full_tile) {
+          if (!full) {
             p0 = 2 * i < lim ? p0 : 0.f;
             p1 = 2 * i + 1 < lim ? p1 : 0.f;
           }
@@ -628,133 +675,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        if constexpr (!kFp8) {
-          // bf16 keeps 8 significant bits.  Where one key carries a sizeable
-          // share of a row's weight (more than 1/64 of the row sum so far),
-          // the rounding would show in O, so the warp's rows also get a
-          // second bf16 term with what the first rounded away (P = P_hi + P_lo
-          // to ~16 bits) and the MMA warp adds a second PV for the tile.
-          // Elsewhere the rounding errors of many small weights average out.
-          const float pmax = lim > 0 ? fast_exp2(mt - m_run) : 0.f;
-          heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
-          if (heavy) {  // warp-uniform
-#pragma unroll
-            for (int i = 0; i < T / 2; ++i) {
-              const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-              pk[32 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
-            }
-          }
-        }
-        if (!heavy) {
-#pragma unroll
-          for (int i = 0; i < T / 2; ++i) pk[32 + i] = 0u;
-        }
-        // Weights, rescale factor and (lane 0) a header to the partner's
-        // helper warp for these rows; the low-order terms only when heavy.
-        const uint32_t dst = peer_x + 2 * RECV_S + p_off;
-        const uint32_t bar_p = ptx::mapa(ptx::smem_u32(&bars.recvp_full[buf][pair]), peer);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          ptx::st_async_u4(dst + RP_HI + (q * 32 + lane) * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                           pk[4 * q + 3], bar_p);
-        ptx::st_async_b32(dst + RP_ALPHA + lane * 4, __float_as_uint(alpha), bar_p);
-        if (lane == 0) ptx::st_async_u4(dst + RP_HDR, heavy ? 1u : 0u, 0u, 0u, 0u, bar_p);
-        if (heavy) {
-          const uint32_t bar_lo = ptx::mapa(ptx::smem_u32(&bars.recvlo_full[buf][pair]), peer);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            ptx::st_async_u4(dst + RP_LO + (q * 32 + lane) * 16, pk[32 + 4 * q], pk[33 + 4 * q],
-                             pk[34 + 4 * q], pk[35 + 4 * q], bar_lo);
-        }
-      } else {
-        // ---- helper: my partial scores of the partner's rows go out ...
-        const uint32_t dst = peer_x + buf * RECV_S;
-        const uint32_t bar_s = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf]), peer);
-#pragma unroll
-        for (int q = 0; q < T / 4; ++q)
-          ptx::st_async_v4(dst + (q * 64 + orow) * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2],
-                           s[4 * q + 3], bar_s);
-        // ... and their weights come back
-        const uint32_t rp = ptx::smem_u32(&bars.recvp_full[buf][pair]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(rp, kPBytes);
-        if (!wait_all<false>(c, rp, (t >> 1) & 1)) { ok = false; break; }
-        const uint32_t src = x_p + p_off;
-        heavy = ld_shared_u4(src + RP_HDR).x != 0;
-        alpha = __uint_as_float(ld_shared_u32(src + RP_ALPHA + lane * 4));
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = ld_shared_u4(src + RP_HI + (q * 32 + lane) * 16);
-          pk[4 * q] = v.x;
-          pk[4 * q + 1] = v.y;
-          pk[4 * q + 2] = v.z;
-          pk[4 * q + 3] = v.w;
-        }
-        const uint32_t rlo = ptx::smem_u32(&bars.recvlo_full[buf][pair]);
+      }
+      // The P columns of this tile: keys 32g.. as 16-bit pairs at 16g, and
+      // (bf16) their low-order terms at 32 + 16g.  Both siblings have read
+      // their scores (the max swap came after), so neither overwrites the
+      // other's unread scores.
+      const uint32_t pcol = tmem + lanes + TM_S + buf * T;
+      ptx::tmem_st16(pcol + g * 16, pk);
+      if constexpr (!kFp8) {
+        // bf16 keeps 8 significant bits.  Where one key carries a sizeable
+        // share of a row's weight (more than 1/64 of this warp's row sum so
+        // far), the rounding would show in O, so the warp's rows also get a
+        // second bf16 term with what the first rounded away (P = P_hi + P_lo
+        // to ~16 bits) and the MMA warp adds a second PV for the tile.
+        // Elsewhere the rounding errors of many small weights average out.
+        // Each warp votes with one byte; a warp that votes no writes zeros as
+        // its second term, so the second PV is right whichever warps voted.
+        const float pmax = lim > 0 ? fast_exp2(fmaf(my_mx, c2, neg_m)) : 0.f;
+        const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
         if (heavy) {  // warp-uniform
-          if (lane == 0) ptx::mbar_arrive_expect_tx(rlo, 32 * 128);
-          if (!wait_all<false>(c, rlo, (t >> 1) & 1)) { ok = false; break; }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 v = ld_shared_u4(src + RP_LO + (q * 32 + lane) * 16);
-            pk[32 + 4 * q] = v.x;
-            pk[33 + 4 * q] = v.y;
-            pk[34 + 4 * q] = v.z;
-            pk[35 + 4 * q] = v.w;
+          for (int i = 0; i < 16; ++i) {
+            const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
+            pk[16 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
           }
         } else {
-          if (lane == 0) ptx::mbar_arrive(rlo);  // no low-order terms this tile
 #pragma unroll
-          for (int i = 0; i < T / 2; ++i) pk[32 + i] = 0u;
+          for (int i = 0; i < 16; ++i) pk[16 + i] = 0u;
         }
+        ptx::tmem_st16(pcol + 32 + g * 16, pk + 16);
+        if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = heavy ? 1 : 0;
       }
-      // Rescale this CTA's half of O for these rows (the PV of the previous
-      // tile must have finished accumulating).
-      if (__any_sync(0xffffffffu, alpha != 1.f) && t > 0) {
-        if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          ptx::tmem_st32(tmem + lanes + TM_O + ch * 32, o);
-        }
-      }
-      ptx::tmem_st64(tmem + lanes + TM_S + buf * T, pk);
-      if (!kFp8 && lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[q4] = heavy ? 1 : 0;
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
+      // This warp's receive buffer of tile t is read (its values went into
+      // the weights just stored): tell the partner warp, unless it has no
+      // tile t + 2 to send.
+      if (t + 2 < n_tiles) {
+        __syncwarp();
+        if (lane == 0)
+          ptx::st_async_b32(peer_free + buf * 32, 0u,
+                            ptx::mapa(ptx::smem_u32(&bars.recv_free[buf][sw]), peer));
+      }
       ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
     }
 
     // ---------------------------------------------------------- epilogue ---
-    // Owners know 1/l of their rows and send it to the partner's helpers.
-    float inv = 0.f;
+    // Row sum = the two siblings' sums, added in the same order by both.
+    float inv = 0.f, l_tot = 0.f;
     if (ok) {
-      if (owner) {
-        inv = l_run > 0.f ? s_kv / l_run : 0.f;
-        ptx::st_async_b32(peer_x + 2 * RECV_S + 4 * RECV_P + pair * RECV_FIN + lane * 4,
-                          __float_as_uint(inv),
-                          ptx::mapa(ptx::smem_u32(&bars.fin_full[pair]), peer));
-      } else {
-        const uint32_t fb = ptx::smem_u32(&bars.fin_full[pair]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, RECV_FIN);
-        ok = wait_all<false>(c, fb, 0);
-        if (ok) inv = __uint_as_float(ld_shared_u32(x_fin + pair * RECV_FIN + lane * 4));
+      const uint32_t x_l = sbase + OFF_RECV + X_L;
+      st_shared_f32(x_l + (g * 128 + r) * 4, l_run);
+      const uint32_t xb = ptx::smem_u32(&bars.xl_full[q4]);
+      ptx::mbar_arrive(xb);
+      ok = wait_all<false>(c, xb, 0);
+      if (ok) {
+        const float other = ld_shared_f32(x_l + ((g ^ 1) * 128 + r) * 4);
+        l_tot = g == 0 ? l_run + other : other + l_run;
+        inv = l_tot > 0.f ? s_kv / l_tot : 0.f;
       }
     }
     if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
       ptx::tc_fence_after();
       const bool single = p.num_splits == 1;
-      uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
+      const int dim0 = vdim0 + g * 128;  // this warp's 128 output dims
+      uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + dim0);
       const size_t prow = ((size_t)b * p.num_splits + split) * p.rows + row;
-      float4* o_f32 = single ? nullptr : reinterpret_cast<float4*>(p.part_o + prow * mla::kDV + vdim0);
+      float4* o_f32 = single ? nullptr : reinterpret_cast<float4*>(p.part_o + prow * mla::kDV + dim0);
 #pragma unroll 1
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int ch = 0; ch < 4; ++ch) {
         uint32_t o[32];
-        ptx::tmem_ld32(tmem + lanes + TM_O + ch * 32, o);
+        ptx::tmem_ld32(tmem + lanes + TM_O + g * 128 + ch * 32, o);
         ptx::tmem_ld_wait();
         if (!valid_row) continue;
         if (single) {
@@ -775,8 +766,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (valid_row && owner) {
-        const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      if (valid_row && rank == 0 && g == 0) {
+        const float lse = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
         if (single) p.lse[(size_t)b * p.rows + row] = lse;
         else p.part_lse[prow] = lse;
       }
