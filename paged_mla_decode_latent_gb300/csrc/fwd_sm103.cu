@@ -735,6 +735,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         inv = l_tot > 0.f ? s_kv / l_tot : 0.f;
       }
     }
+    // O is final once the last PV has drained.  A parity wait only tells the
+    // current phase from the one before it, and the PV of the previous tile
+    // may not be issued yet (other lane quarters can still be on it), so the
+    // two last phases are waited for in order.
+    if (ok && n_tiles >= 2)
+      ok = wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 2) & 1);
     if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
       ptx::tc_fence_after();
       const bool single = p.num_splits == 1;
