@@ -117,6 +117,7 @@ struct Bars {
   uint64_t xm_full[2][4];                // both sibling warps of a lane quarter wrote their maxima
   uint64_t xl_full[4];                   // both sibling warps wrote their row sums
   uint64_t o_done;
+  uint64_t o_final;  // the last PV has drained (one phase)
   uint64_t q_ready;
   uint64_t drain;
   uint32_t tmem_base;
@@ -317,6 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xl_full[q]), 64);
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars.o_final), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * kSoftmaxWarps);
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
     bars.abort = 0;
@@ -364,6 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, vmajor_desc(st + kk * 2048), id_pv, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
+        if (t == n_tiles - 1) ptx::mma_commit(ptx::smem_u32(&bars.o_final));
         ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
       };
       // Issue whichever is ready: QK^T of tile nq (its stage has landed and
@@ -735,13 +738,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         inv = l_tot > 0.f ? s_kv / l_tot : 0.f;
       }
     }
-    // O is final once the last PV has drained.  A parity wait only tells the
-    // current phase from the one before it, and the PV of the previous tile
-    // may not be issued yet (other lane quarters can still be on it), so the
-    // two last phases are waited for in order.
-    if (ok && n_tiles >= 2)
-      ok = wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 2) & 1);
-    if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_done), (n_tiles - 1) & 1)) {
+    // O is final once the last PV has drained.  It has a barrier of its own:
+    // a parity wait on o_done only tells the current phase from the one
+    // before it, and here o_done may be one phase short (another lane
+    // quarter still holds back the previous PV) or already complete.
+    if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_final), 0)) {
       ptx::tc_fence_after();
       const bool single = p.num_splits == 1;
       const int dim0 = vdim0 + g * 128;  // this warp's 128 output dims
