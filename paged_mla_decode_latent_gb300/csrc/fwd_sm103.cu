@@ -9,7 +9,8 @@
 // 64 rope dims).  Each CTA therefore reads only its part of every latent row.
 //
 // Per 64-key tile, in each CTA:
-//   loader warps  : three warps take turns by tile: block-table lookup, then
+//   loader warps  : four (bf16) or three (fp8) warps take turns by tile, one per
+//                   operand stage: block-table lookup, then
 //                   16-byte cp.async of the tile's rows in 128-byte pieces
 //                   (one 64-dim slab of one key) straight into a 128B-swizzled
 //                   K-major stage (bf16), or into a raw stage the same lanes
@@ -21,11 +22,12 @@
 //                   stage read MN-major as V).
 //   softmax warps : eight warps, two per TMEM lane quarter; of each tile the
 //                   first reads keys 0..31 of its 32 rows, the second keys
-//                   32..63.  Each sends its block of partial scores to the
-//                   same warp of the partner CTA over distributed shared
-//                   memory (st.async counted on the partner's mbarrier),
-//                   adds the partner's block (a + b in one CTA, b + a in the
-//                   other: bit-identical sums), swaps its row maxima with
+//                   32..63.  Each rounds its partial scores to 24 bits,
+//                   sends the packed block to the same warp of the partner
+//                   CTA over distributed shared memory (st.async counted on
+//                   the partner's mbarrier), adds the partner's block (a + b
+//                   in one CTA, b + a in the other: bit-identical sums, so
+//                   both CTAs take the same decisions), swaps its row maxima with
 //                   its sibling warp, then runs the online softmax with a
 //                   lazily rescaled running max and writes its weights to
 //                   TMEM over the consumed score columns (bf16: a high part
@@ -67,25 +69,28 @@ constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
 // Exchange with the partner CTA: each softmax warp sends and receives one
-// 32-row x 32-key block of fp32 partial scores per tile.
+// 32-row x 32-key block of partial scores per tile, each score rounded to
+// 24 bits (16 significant bits) and packed four to three words.
 constexpr int kSoftmaxWarps = 8;
-constexpr int RECV_W = 32 * 32 * 4;                  // one warp's block (4 KB)
-constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (32 KB)
-constexpr int X_FREE = 2 * RECV;                     // [2][8] words the "buffer free" signals land in
+constexpr int RECV_W = 32 * 32 * 3;                  // one warp's block (3 KB)
+constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (24 KB), one buffer
+constexpr int X_FREE = RECV;                         // [8] words the "buffer free" signals land in
 constexpr int X_MAX = X_FREE + 128;                  // [2 bufs][2 key halves][128 rows] row maxima
 constexpr int X_L = X_MAX + 2 * 2 * 128 * 4;         // [2 key halves][128 rows] row sums
 constexpr int XCHG = X_L + 2 * 128 * 4;
-constexpr int kThreads = 128 + 32 * kSoftmaxWarps;  // 12 warps
-constexpr int kSoftmaxWarp0 = 4;       // warps 4-11; warps 2, 3, 0 load; warp 1 issues MMAs
+// Warps: 0..3 loaders (warp w owns operand stage w), 4..11 softmax, 12 MMA.
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 32 * 13;
 
 // Shared-memory plan.  Each operand stage has its own loader warp, so every
-// stage barrier is waited on by one warp, in order.  bf16 cache: 3 operand
-// stages filled with cp.async.  fp8 cache: 2 f16 operand stages, each with a
+// stage barrier is waited on by one warp, in order.  bf16 cache: 4 operand
+// stages filled with cp.async.  fp8 cache: 3 f16 operand stages, each with a
 // raw stage of codes its loader warp copies into and converts from.
 template <bool kFp8>
 struct Layout {
-  static constexpr int NS = kFp8 ? 2 : 3;   // operand stages = loader warps
-  static constexpr int NR = kFp8 ? 2 : 0;   // raw fp8 stages (one per loader warp)
+  static constexpr int NS = kFp8 ? 3 : 4;   // operand stages = loader warps
+  static constexpr int NR = kFp8 ? 3 : 0;   // raw fp8 stages (one per loader warp)
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
@@ -108,12 +113,12 @@ constexpr float kMaxSentinel = -1.0e30f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 struct Bars {
-  uint64_t kv_full[3];    // operand stage ready (the 32 threads of its loader warp arrive)
-  uint64_t kv_empty[3];   // operand stage consumed by the MMAs
+  uint64_t kv_full[4];    // operand stage ready (the 32 threads of its loader warp arrive)
+  uint64_t kv_empty[4];   // operand stage consumed by the MMAs
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t recv_full[2][kSoftmaxWarps];  // the partner warp's partial scores landed (4 KB)
-  uint64_t recv_free[2][kSoftmaxWarps];  // the partner warp has read what this warp sent
+  uint64_t recv_full[kSoftmaxWarps];  // the partner warp's partial scores landed (3 KB)
+  uint64_t recv_free[kSoftmaxWarps];  // the partner warp has read what this warp sent
   uint64_t xm_full[2][4];                // both sibling warps of a lane quarter wrote their maxima
   uint64_t xl_full[4];                   // both sibling warps wrote their row sums
   uint64_t o_done;
@@ -197,6 +202,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return r;
 }
 
+// fp32 -> the same value rounded to 16 significant bits (round half away
+// from zero on the magnitude), low 8 bits zero.
+__device__ __forceinline__ uint32_t round24(float x) {
+  return (__float_as_uint(x) + 0x80u) & 0xFFFFFF00u;
+}
+
+// Four values with zero low bytes -> three words (their upper three bytes).
+__device__ __forceinline__ void pack24(float a, float b, float c, float d, uint32_t* w) {
+  const uint32_t A = __float_as_uint(a), B = __float_as_uint(b), C = __float_as_uint(c),
+                 D = __float_as_uint(d);
+  w[0] = __byte_perm(A, B, 0x5321);
+  w[1] = __byte_perm(B, C, 0x6532);
+  w[2] = __byte_perm(C, D, 0x7653);
+}
+
+__device__ __forceinline__ void unpack24(const uint32_t* w, float* u) {
+  u[0] = __uint_as_float(__byte_perm(w[0], 0u, 0x2104));
+  u[1] = __uint_as_float(__byte_perm(w[0], w[1], 0x5430) & 0xFFFFFF00u);
+  u[2] = __uint_as_float(__byte_perm(w[1], w[2], 0x4320) & 0xFFFFFF00u);
+  u[3] = __uint_as_float(w[2] & 0xFFFFFF00u);
+}
+
 __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -219,15 +246,6 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
   return v;
 }
 
@@ -310,13 +328,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * kSoftmaxWarps);
-      for (int w = 0; w < kSoftmaxWarps; ++w) {
-        ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i][w]), 1);
-        ptx::mbar_init(ptx::smem_u32(&bars.recv_free[i][w]), 1);
-      }
       for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xm_full[i][q]), 64);
     }
     for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xl_full[q]), 64);
+    for (int w = 0; w < kSoftmaxWarps; ++w) {
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[w]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_free[w]), 1);
+    }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.o_final), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * kSoftmaxWarps);
@@ -324,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars.tmem_base), TM_COLS);
     ptx::tmem_relinquish();
   }
@@ -334,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort};
 
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
       const uint32_t id_qk = ptx::idesc_f16(128, T, kAB, false, false);
@@ -393,7 +411,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (progress) {
           idle = 0;
           t_last = 0;
-        } else if ((++idle & 255) == 0) {
+          continue;
+        }
+        // Nothing ready.  Do not spin on the issue slots the softmax and
+        // loader warps of this sub-partition need: when only the weights of
+        // tile np can unblock the pipe, sleep on their barrier (the phase is
+        // tested again above); otherwise back off briefly.
+        if (nq < n_tiles && nq <= np + 1) __nanosleep(32);
+        else (void)ptx::mbar_try_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1);
+        if ((++idle & 15) == 0) {
           const uint64_t now = ptx::globaltimer_ns();
           if (t_last == 0) t_last = now;
           if (*c.abort) ok = false;
@@ -407,14 +433,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3 || (warp == 0 && NS == 3)) {
+  } else if (warp < NS) {
     // ------------------------------------------------------------ loader ---
     // Gather of a tile's cache rows with 16-byte cp.async (L2 only).  The
     // operand layout keeps a key's 64-dim slab contiguous only over 128 B, so
     // every copy is a 128-byte piece of one row: 8 lanes per (key, slab)
     // piece for bf16, written straight into the 128B-swizzled stage; 4 lanes
     // per 64-byte piece of fp8 codes, written into the warp's raw stage and
-    // converted to f16 by the same lanes.  Loader warp w (warps 2, 3, 0)
+    // converted to f16 by the same lanes.  Loader warp w
     // owns operand stage w and copies tiles w, w+NS, ...: it issues a tile,
     // waits for its own copies, fences them for the tensor cores' async proxy
     // and arrives on the stage's full barrier, while the other loader warps
@@ -423,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int LPI = kFp8 ? 4 : 8;        // lanes per piece
     constexpr int IPI = 32 / LPI;            // pieces per warp instruction
     constexpr int NK = T / IPI;              // keys per lane: 16 (bf16) or 8 (fp8)
-    const int lw = warp == 0 ? 2 : warp - 2;  // 0, 1, 2: the operand stage this warp owns
+    const int lw = warp;  // the operand stage this warp owns
     const int g = lane / LPI, sub = lane % LPI;
     const int n_slots = rank == 0 ? 5 : 4;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
@@ -505,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
     }
     ptx::cp_async_wait<0>();  // nothing of this warp is in flight when it leaves
-  } else if (warp >= kSoftmaxWarp0) {
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + kSoftmaxWarps) {
     // ----------------------------------------------------------- softmax ---
     // Softmax warp sw (0..7) reads TMEM lane quarter q4 = warp % 4 (rows
     // 32 q4 .. 32 q4 + 31 of the block) and owns key half g = sw / 4 of every
@@ -564,14 +590,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
     float m_run = kMaxSentinel;  // running max (log2 domain), the same in both siblings
     float l_run = 0.f;           // exact row sum over this warp's keys only
-    const uint32_t my_recv = sbase + OFF_RECV + sw * RECV_W;  // + buf * RECV
+    const uint32_t my_recv = sbase + OFF_RECV + sw * RECV_W;
     const uint32_t peer_recv = ptx::mapa(my_recv, peer);
-    const uint32_t peer_free = ptx::mapa(sbase + OFF_RECV + X_FREE + sw * 4, peer);  // + buf * 32
+    const uint32_t peer_free = ptx::mapa(sbase + OFF_RECV + X_FREE + sw * 4, peer);
+    const uint32_t recv_full = ptx::smem_u32(&bars.recv_full[sw]);
+    const uint32_t recv_free = ptx::smem_u32(&bars.recv_free[sw]);
     const uint32_t x_max = sbase + OFF_RECV + X_MAX;
+    // A lane quarter with no row of the problem (fewer than 128 rows) swaps
+    // nothing and computes nothing; its warps only keep the barrier phases
+    // moving.  Both CTAs skip the same quarters.  Its TMEM lanes hold garbage
+    // that no output reads (the MMAs keep rows apart).
+    const bool live = rb * mla::kRowTile + q4 * 32 < p.rows;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       if (!wait_all<false>(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
+      if (!live) {
+        if (!kFp8 && lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = 0;
+        ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
+        continue;
+      }
       ptx::tc_fence_after();
       float s[32];
       {
@@ -581,34 +619,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
       }
-      // Swap partial-score blocks with the same warp of the partner CTA.  The
-      // block of tile t goes into the partner's buffer t % 2 once the partner
-      // has read what this warp put there for tile t - 2.
-      if (t >= 2) {
-        const uint32_t fb = ptx::smem_u32(&bars.recv_free[buf][sw]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, 4);
-        if (!wait_all<false>(c, fb, ((t >> 1) - 1) & 1)) { ok = false; break; }
+      // Swap partial-score blocks with the same warp of the partner CTA.
+      // Both CTAs round their own partial scores to 24 bits too, so that the
+      // sums are bit-identical.  The block of tile t goes into the partner's
+      // (single) buffer once the partner has read tile t - 1 from it.
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(round24(s[i]));
+      if (t >= 1) {
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_free, 4);
+        if (!wait_all<false>(c, recv_free, (t - 1) & 1)) { ok = false; break; }
       }
       {
-        const uint32_t dst = peer_recv + buf * RECV + lane * 16;
-        const uint32_t bar = ptx::mapa(ptx::smem_u32(&bars.recv_full[buf][sw]), peer);
+        const uint32_t dst = peer_recv + lane * 16;
+        const uint32_t bar = ptx::mapa(recv_full, peer);
 #pragma unroll
-        for (int qd = 0; qd < 8; ++qd)
-          ptx::st_async_v4(dst + qd * 512, s[4 * qd], s[4 * qd + 1], s[4 * qd + 2], s[4 * qd + 3], bar);
-      }
-      {
-        const uint32_t rf = ptx::smem_u32(&bars.recv_full[buf][sw]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(rf, RECV_W);
-        if (!wait_all<false>(c, rf, (t >> 1) & 1)) { ok = false; break; }
-        const uint32_t src = my_recv + buf * RECV + lane * 16;
+        for (int qd = 0; qd < 2; ++qd) {  // 16 scores -> 12 words -> 3 stores
+          uint32_t w[12];
 #pragma unroll
-        for (int qd = 0; qd < 8; ++qd) {
-          const float4 v = ld_shared_v4(src + qd * 512);
-          s[4 * qd] += v.x;
-          s[4 * qd + 1] += v.y;
-          s[4 * qd + 2] += v.z;
-          s[4 * qd + 3] += v.w;
+          for (int k = 0; k < 4; ++k)
+            pack24(s[16 * qd + 4 * k], s[16 * qd + 4 * k + 1], s[16 * qd + 4 * k + 2],
+                   s[16 * qd + 4 * k + 3], w + 3 * k);
+#pragma unroll
+          for (int v = 0; v < 3; ++v)
+            ptx::st_async_u4(dst + (3 * qd + v) * 512, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                             w[4 * v + 3], bar);
         }
+      }
+      {
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
+        if (!wait_all<false>(c, recv_full, t & 1)) { ok = false; break; }
+        const uint32_t src = my_recv + lane * 16;
+        uint32_t fold = 0;
+#pragma unroll
+        for (int qd = 0; qd < 2; ++qd) {
+          uint32_t w[12];
+#pragma unroll
+          for (int v = 0; v < 3; ++v) {
+            const uint4 x = ld_shared_u4(src + (3 * qd + v) * 512);
+            w[4 * v] = x.x;
+            w[4 * v + 1] = x.y;
+            w[4 * v + 2] = x.z;
+            w[4 * v + 3] = x.w;
+            fold ^= x.x ^ x.y ^ x.z ^ x.w;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float u[4];
+            unpack24(w + 3 * k, u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[16 * qd + 4 * k + e] += u[e];
+          }
+        }
+        // The buffer is read (the vote needs every lane's loaded words): the
+        // partner may send its next tile.
+        const bool any = __any_sync(0xffffffffu, fold == 0x9E3779B9u);
+        if (t + 1 < n_tiles && lane == 0)
+          ptx::st_async_b32(peer_free, any ? 1u : 0u, ptx::mapa(recv_free, peer));
       }
       // Row max over this warp's visible keys, then over both halves of the
       // tile (swapped with the sibling warp).  Only the last tile of a split
@@ -711,21 +777,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      // This warp's receive buffer of tile t is read (its values went into
-      // the weights just stored): tell the partner warp, unless it has no
-      // tile t + 2 to send.
-      if (t + 2 < n_tiles) {
-        __syncwarp();
-        if (lane == 0)
-          ptx::st_async_b32(peer_free + buf * 32, 0u,
-                            ptx::mapa(ptx::smem_u32(&bars.recv_free[buf][sw]), peer));
-      }
       ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
     }
 
     // ---------------------------------------------------------- epilogue ---
     // Row sum = the two siblings' sums, added in the same order by both.
     float inv = 0.f, l_tot = 0.f;
+    if (!live) ok = false;  // nothing to write
     if (ok) {
       const uint32_t x_l = sbase + OFF_RECV + X_L;
       st_shared_f32(x_l + (g * 128 + r) * 4, l_run);
@@ -784,7 +842,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------ teardown ---
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     if (bars.abort) {
       // wait for every tcgen05 op this CTA issued before giving TMEM back
       if (lane == 0) {
