@@ -110,7 +110,8 @@ typedef struct mla_decode_plan_t {
   int32_t num_splits;   /* splits per sequence = ceil(max_ctx / chunk_len) */
   int32_t num_sms;      /* SM count the partition was balanced for */
   int32_t cluster_size; /* CTAs cooperating on one (b, row block, split) */
-  int32_t grid_x, grid_y, grid_z; /* launch grid of mla_decode_fwd */
+  int32_t grid_x, grid_y, grid_z; /* launch grid of mla_decode_fwd: (2 x row_blocks, batch,
+                                     num_splits); splits vary slowest */
   int32_t reserved0;
   int64_t ws_partial_o_offset;   /* byte offset of fp32 [B, S, rows, 512] partials */
   int64_t ws_partial_lse_offset; /* byte offset of fp32 [B, S, rows] partial LSEs */

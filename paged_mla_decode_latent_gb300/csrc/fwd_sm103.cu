@@ -1,7 +1,7 @@
 // fwd_sm103.cu -- the decode kernel on the 5th-generation tensor cores.
 //
 // Work unit: one (sequence b, 128-row block, KV split) handled by a cluster of
-// two CTAs.  Rows are the Sq*H query rows of the sequence (token-major, as q
+// two CTAs; grid (2 x row blocks, sequences, splits).  Rows are the Sq*H query rows of the sequence (token-major, as q
 // is laid out), padded to the MMA M of 128.  The fp32 output accumulator of
 // 128 rows x 512 value dims would fill all 512 TMEM columns of one SM, so the
 // two CTAs split the value dims: CTA r owns value dims [256r, 256r+256) and,
@@ -289,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int split = blockIdx.x >> 1, rb = blockIdx.y, b = blockIdx.z;
+  const int rb = blockIdx.x >> 1, b = blockIdx.y, split = blockIdx.z;
 
   int ctx = p.seq_lens[b];
   const int covered = p.num_splits * p.chunk_len;
@@ -869,7 +869,9 @@ int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
     if (e != cudaSuccess) return (int)e;
     attr_done[fp8] = true;
   }
-  dim3 grid(p.num_splits * 2, p.row_blocks, p.batch);
+  // Splits vary slowest, so every sequence's first chunk is dispatched
+  // before any second chunk (the planner simulates this order).
+  dim3 grid(p.row_blocks * 2, p.batch, p.num_splits);
   kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return (int)cudaGetLastError();
 }

@@ -40,9 +40,11 @@ double simulate(const int32_t* lens, int batch, int row_blocks, int chunk, int s
   std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
   for (int p = 0; p < pairs; ++p) free_at.push(0.0);
   double makespan = 0.0;
-  for (int b = 0; b < batch; ++b) {
-    for (int rb = 0; rb < row_blocks; ++rb) {
-      for (int s = 0; s < splits; ++s) {
+  // Dispatch order of the launch grid (2 x row blocks, batch, splits): the
+  // row block varies fastest, the split slowest.
+  for (int s = 0; s < splits; ++s) {
+    for (int b = 0; b < batch; ++b) {
+      for (int rb = 0; rb < row_blocks; ++rb) {
         int64_t lo = (int64_t)s * chunk;
         int64_t keys = std::max<int64_t>(0, std::min<int64_t>(lens[b], lo + chunk) - lo);
         double cost = keys > 0 ? ns_fixed + keys * ns_per_key + (splits > 1 ? ns_partial : 0.0)
@@ -55,7 +57,7 @@ double simulate(const int32_t* lens, int batch, int row_blocks, int chunk, int s
       }
     }
   }
-  return makespan + (splits > 1 ? ns_combine : 0.0);
+  return makespan + (splits > 1 ? ns_combine * splits : 0.0);
 }
 
 }  // namespace
@@ -99,46 +101,67 @@ extern "C" int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int3
   p.num_sms = num_sms;
   p.cluster_size = mla::kClusterSize;
 
-  // Per-pair cost model.  A pair streams keys at its share of HBM bandwidth,
-  // or at its share of the tensor rate when that is slower (fp8 at 128 rows).
+  // Per-pair cost model of the decode kernel on GB300.  Its pipeline is bound
+  // by the latency of its per-tile chain (score contraction, score swap between
+  // the two CTAs, softmax, value contraction), not by its share of HBM
+  // bandwidth, so a pair's time per key does not depend on how many pairs run:
+  // about 2.2 us per 64-key tile measured for 128 rows, bf16 or fp8.  A work
+  // unit also pays its prologue, pipeline fill and epilogue (about 10 us), a
+  // split result its partial write, and a split launch the combine pass over
+  // all partials.
   const int pairs = std::max(1, num_sms / p.cluster_size);
-  const double hbm_bytes_per_ns = 6700.0, tc_flop_per_ns = 1.9e6;
-  const double key_bytes = kv_dtype == MLA_KV_BF16 ? 1152.0 : 576.0;
-  const double rows_pad = (double)p.row_tile;
-  const double ns_key_hbm = key_bytes * pairs / hbm_bytes_per_ns;
-  const double ns_key_tc = 2.0 * rows_pad * (MLA_D_QK + MLA_D_V) * pairs / tc_flop_per_ns;
-  const double ns_per_key = std::max(ns_key_hbm, ns_key_tc);
-  const double ns_fixed = 2000.0, ns_empty = 400.0, ns_combine = 4000.0;
-  const double partial_bytes = 2.0 * std::min(p.rows, p.row_tile) * (MLA_D_V * 4.0 + 4.0);
-  const double ns_partial = partial_bytes * pairs / hbm_bytes_per_ns;
-
+  const double ns_per_key = 2200.0 / p.key_tile;
+  const double ns_fixed = 10000.0, ns_empty = 400.0, ns_partial = 1000.0;
+  const double partial_bytes_total =
+      (double)batch * std::min(p.rows, p.row_tile * p.row_blocks) * (MLA_D_V * 4.0 + 4.0);
+  // The combine reads every split's partials once (about 5000 bytes/ns) after a
+  // launch gap; charged per split so that the simulation can add it up.
+  const double ns_combine_per_split = 1500.0 + partial_bytes_total / 5000.0;
   int best_chunk = (int)round_up(std::max(max_ctx, 1), p.key_tile);
   int best_splits = 1;
   if (max_ctx > 0) {
     double best_t = simulate(seq_lens_host, batch, p.row_blocks, best_chunk, 1, pairs, ns_per_key,
-                             ns_fixed, ns_partial, ns_empty, ns_combine);
+                             ns_fixed, ns_partial, ns_empty, ns_combine_per_split);
     const int64_t max_splits =
         std::min<int64_t>(ceil_div(max_ctx, p.key_tile), mla::kMaxSplits);
+    auto consider = [&](int chunk) {
+      const int splits = (int)ceil_div(max_ctx, chunk);
+      if (splits < 2 || splits > mla::kMaxSplits) return;
+      double t = simulate(seq_lens_host, batch, p.row_blocks, chunk, splits, pairs, ns_per_key,
+                          ns_fixed, ns_partial, ns_empty, ns_combine_per_split);
+      // A split must promise a clear gain: the model leaves out that the
+      // pairs slow down a little when all of them run, and short tail units
+      // fill their pipelines less well (measured: a 113 + 15 tile split of
+      // batch 64 x 8192 was 10% slower than one unit per sequence).
+      if (t < best_t * 0.9) {
+        best_t = t;
+        best_chunk = chunk;
+        best_splits = splits;
+      }
+    };
+    // Even splits of the longest context ...
     int last_splits = 1;
     for (int64_t s = 2; s <= max_splits; ++s) {
       int chunk = (int)round_up(ceil_div(max_ctx, s), p.key_tile);
       int splits = (int)ceil_div(max_ctx, chunk);
       if (splits == last_splits) continue;
       last_splits = splits;
-      double t = simulate(seq_lens_host, batch, p.row_blocks, chunk, splits, pairs, ns_per_key,
-                          ns_fixed, ns_partial, ns_empty, ns_combine);
-      if (t < best_t * 0.99) {
-        best_t = t;
-        best_chunk = chunk;
-        best_splits = splits;
-      }
+      consider(chunk);
     }
+    // ... and, for short contexts, every chunk between half and all of it: a
+    // long first chunk and a short tail lets the tails of all sequences fill
+    // the SM pairs the first chunks leave idle (first chunks are dispatched
+    // first).
+    if (max_ctx <= 32768)
+      for (int64_t chunk = round_up(ceil_div(max_ctx, 2), p.key_tile); chunk < max_ctx;
+           chunk += p.key_tile)
+        consider((int)chunk);
   }
   p.chunk_len = best_chunk;
   p.num_splits = best_splits;
-  p.grid_x = p.num_splits * p.cluster_size;
-  p.grid_y = p.row_blocks;
-  p.grid_z = batch;
+  p.grid_x = p.row_blocks * p.cluster_size;
+  p.grid_y = batch;
+  p.grid_z = p.num_splits;
 
   int64_t off = 0;
   if (p.num_splits > 1) {

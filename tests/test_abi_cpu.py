@@ -64,7 +64,7 @@ def check_plan_invariants(p, lens):
     assert p.num_splits * p.chunk_len >= lens.max()
     assert (p.num_splits - 1) * p.chunk_len < max(1, lens.max())
     assert p.rows == p.num_heads * p.sq and p.row_blocks == -(-p.rows // 128)
-    assert (p.grid_x, p.grid_y, p.grid_z) == (2 * p.num_splits, p.row_blocks, len(lens))
+    assert (p.grid_x, p.grid_y, p.grid_z) == (2 * p.row_blocks, len(lens), p.num_splits)
     assert p.ws_status_offset % 256 == 0 and p.workspace_bytes % 256 == 0
     if p.num_splits > 1:
         o_bytes = len(lens) * p.num_splits * p.rows * 512 * 4
