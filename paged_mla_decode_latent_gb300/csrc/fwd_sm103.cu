@@ -20,19 +20,18 @@
 //                   CTA 0's rope part A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
 //                   stage read MN-major as V).
-//   softmax warps : eight warps, two per TMEM lane quarter; of each tile the
-//                   first reads keys 0..31 of its 32 rows, the second keys
-//                   32..63.  Each rounds its partial scores to 24 bits,
-//                   sends the packed block to the same warp of the partner
-//                   CTA over distributed shared memory (st.async counted on
-//                   the partner's mbarrier), adds the partner's block (a + b
-//                   in one CTA, b + a in the other: bit-identical sums, so
-//                   both CTAs take the same decisions), swaps its row maxima with
-//                   its sibling warp, then runs the online softmax with a
-//                   lazily rescaled running max and writes its weights to
-//                   TMEM over the consumed score columns (bf16: a high part
-//                   and, on tiles where one key carries much of a row's
-//                   weight, a low part).
+//   softmax warps : eight warps of 16 whole rows each (TMEM 16-lane access
+//                   shapes; a row's keys spread over a quad of threads).
+//                   Each rounds its partial scores to 24 bits, sends the
+//                   packed block to the same warp of the partner CTA over
+//                   distributed shared memory (st.async counted on the
+//                   partner's mbarrier), adds the partner's block (a + b in
+//                   one CTA, b + a in the other: bit-identical sums, so both
+//                   CTAs take the same decisions), then runs the online
+//                   softmax with a lazily rescaled running max and writes its
+//                   weights to TMEM over the consumed score columns (bf16: a
+//                   high part and, on tiles where one key carries much of a
+//                   row's weight, a low part).
 // The epilogue normalises O and writes bf16 output (one split) or fp32
 // partials plus the per-row log-sum-exp (several splits).
 //
@@ -75,9 +74,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int RECV_W = 32 * 32 * 3;                  // one warp's block (3 KB)
 constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (24 KB), one buffer
 constexpr int X_FREE = RECV;                         // [8] words the "buffer free" signals land in
-constexpr int X_MAX = X_FREE + 128;                  // [2 bufs][2 key halves][128 rows] row maxima
-constexpr int X_L = X_MAX + 2 * 2 * 128 * 4;         // [2 key halves][128 rows] row sums
-constexpr int XCHG = X_L + 2 * 128 * 4;
+constexpr int XCHG = X_FREE + 128;
 // Warps: 0..3 loaders (warp w owns operand stage w), 4..11 softmax, 12 MMA.
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kMmaWarp = 12;
@@ -119,8 +116,6 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t recv_full[kSoftmaxWarps];  // the partner warp's partial scores landed (3 KB)
   uint64_t recv_free[kSoftmaxWarps];  // the partner warp has read what this warp sent
-  uint64_t xm_full[2][4];                // both sibling warps of a lane quarter wrote their maxima
-  uint64_t xl_full[4];                   // both sibling warps wrote their row sums
   uint64_t o_done;
   uint64_t o_final;  // the last PV has drained (one phase)
   uint64_t q_ready;
@@ -239,16 +234,6 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // Eight bf16 -> eight f16 (exact for |x| in [2^-14, 65504]; flags larger values).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, bool& out_of_range) {
   uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -328,9 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * kSoftmaxWarps);
-      for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xm_full[i][q]), 64);
     }
-    for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&bars.xl_full[q]), 64);
     for (int w = 0; w < kSoftmaxWarps; ++w) {
       ptx::mbar_init(ptx::smem_u32(&bars.recv_full[w]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.recv_free[w]), 1);
@@ -533,29 +516,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cp_async_wait<0>();  // nothing of this warp is in flight when it leaves
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + kSoftmaxWarps) {
     // ----------------------------------------------------------- softmax ---
-    // Softmax warp sw (0..7) reads TMEM lane quarter q4 = warp % 4 (rows
-    // 32 q4 .. 32 q4 + 31 of the block) and owns key half g = sw / 4 of every
-    // tile.  The two warps of a quarter ("siblings") keep the same running
-    // max for their rows (they swap tile maxima) and separate row sums.
+    // Softmax warp sw (0..7) owns 16 whole rows of the 128-row block: TMEM
+    // lanes lbase .. lbase + 15 with lbase = 32 (warp % 4) + 16 (sw / 4) (a
+    // warp reaches the lane quarter warp % 4 only).  Through the 16x256b
+    // access shape thread i holds rows rA = lbase + i/4 and rB = rA + 8, and
+    // of every 8-key group j the keys 8j + 2(i%4) and 8j + 2(i%4) + 1: a row's
+    // 64 keys are spread over the 4 threads of a quad, whose shuffles give the
+    // row max and sum.  The partner CTA's warp sw holds the same elements.
     const int sw = warp - kSoftmaxWarp0;
     const int q4 = warp & 3;                   // TMEM lane quarter of this warp
-    const int g = sw >> 2;                     // key half: keys 32g .. 32g + 31 of a tile
-    const int r = q4 * 32 + lane;              // row within the 128-row block
-    const int row = rb * mla::kRowTile + r;    // row within the sequence
-    const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
-    const bool valid_row = row < p.rows;
-    int nvis = 0;
-    if (valid_row) {
+    const int g = sw >> 2;                     // which half of the quarter
+    const int lbase = q4 * 32 + g * 16;
+    const int cq = lane & 3;                   // column pair within each 8-key group
+    const int rA = lbase + (lane >> 2), rB = rA + 8;
+    const uint32_t lanes16 = (uint32_t)lbase << 16;
+    auto visible = [&](int r) {  // keys [k0, visible) of this split that row r sees
+      const int row = rb * mla::kRowTile + r;
+      if (row >= p.rows) return 0;
       const int tok = row / p.heads;
-      nvis = p.causal ? ctx - p.sq + tok + 1 : ctx;
+      int nvis = p.causal ? ctx - p.sq + tok + 1 : ctx;
       nvis = max(0, min(nvis, ctx));
-    }
-    const int lim_all = min(nvis, k1);  // keys [k0, lim_all) are visible in this split
+      return min(nvis, k1);
+    };
+    const int visA = visible(rA), visB = visible(rB);
 
-    // Q (this CTA's 256 latent dims) -> TMEM as 16-bit pairs, two 64-dim
-    // chunks per sibling; on CTA 0 the second sibling also puts the 64 rope
-    // dims into shared memory (128B-swizzled K-major).
+    // Q (this CTA's 256 latent dims) -> TMEM as 16-bit pairs: thread i of
+    // the two warps of a lane quarter writes row 32 q4 + i, two 64-dim chunks
+    // each; on CTA 0 the second warp also puts the 64 rope dims into shared
+    // memory (128B-swizzled K-major).
     {
+      const int r = q4 * 32 + lane;
+      const int row = rb * mla::kRowTile + r;
+      const bool valid_row = row < p.rows;
+      const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
       const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.rows + row) * mla::kDQK);
       uint32_t buf[32];
       bool q_range = false;
@@ -588,19 +581,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
-    float m_run = kMaxSentinel;  // running max (log2 domain), the same in both siblings
-    float l_run = 0.f;           // exact row sum over this warp's keys only
+    float mA = kMaxSentinel, mB = kMaxSentinel;  // running maxima (log2 domain), quad-uniform
+    float lA = 0.f, lB = 0.f;                     // exact row sums over this thread's keys
     const uint32_t my_recv = sbase + OFF_RECV + sw * RECV_W;
     const uint32_t peer_recv = ptx::mapa(my_recv, peer);
     const uint32_t peer_free = ptx::mapa(sbase + OFF_RECV + X_FREE + sw * 4, peer);
     const uint32_t recv_full = ptx::smem_u32(&bars.recv_full[sw]);
     const uint32_t recv_free = ptx::smem_u32(&bars.recv_free[sw]);
-    const uint32_t x_max = sbase + OFF_RECV + X_MAX;
-    // A lane quarter with no row of the problem (fewer than 128 rows) swaps
-    // nothing and computes nothing; its warps only keep the barrier phases
-    // moving.  Both CTAs skip the same quarters.  Its TMEM lanes hold garbage
-    // that no output reads (the MMAs keep rows apart).
-    const bool live = rb * mla::kRowTile + q4 * 32 < p.rows;
+    // A warp whose 16 rows are all past the problem's rows (fewer than 128
+    // rows) swaps nothing and computes nothing; it only keeps the barrier
+    // phases moving.  Both CTAs skip the same warps.  Its TMEM lanes hold
+    // garbage that no output reads (the MMAs keep rows apart).
+    const bool live = rb * mla::kRowTile + lbase < p.rows;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
@@ -611,20 +603,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         continue;
       }
       ptx::tc_fence_after();
-      float s[32];
+      const uint32_t scol = tmem + lanes16 + TM_S + buf * T;
+      float s[32];  // s[4j + e]: e = 0, 1 -> row A keys 8j + 2cq + e; e = 2, 3 -> row B
       {
         uint32_t raw[32];
-        ptx::tmem_ld32(tmem + lanes + TM_S + buf * T + g * 32, raw);
+        ptx::tmem_ld16x256b_x8(scol, raw);
         ptx::tmem_ld_wait();
+        // Both CTAs round their own partial scores to 24 bits too, so that
+        // the sums are bit-identical.
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(round24(__uint_as_float(raw[i])));
       }
-      // Swap partial-score blocks with the same warp of the partner CTA.
-      // Both CTAs round their own partial scores to 24 bits too, so that the
-      // sums are bit-identical.  The block of tile t goes into the partner's
-      // (single) buffer once the partner has read tile t - 1 from it.
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(round24(s[i]));
+      // Swap partial-score blocks with the same warp of the partner CTA.  The
+      // block of tile t goes into the partner's (single) buffer once the
+      // partner has read tile t - 1 from it.
       if (t >= 1) {
         if (lane == 0) ptx::mbar_arrive_expect_tx(recv_free, 4);
         if (!wait_all<false>(c, recv_free, (t - 1) & 1)) { ok = false; break; }
@@ -676,103 +668,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (t + 1 < n_tiles && lane == 0)
           ptx::st_async_b32(peer_free, any ? 1u : 0u, ptx::mapa(recv_free, peer));
       }
-      // Row max over this warp's visible keys, then over both halves of the
-      // tile (swapped with the sibling warp).  Only the last tile of a split
-      // and causal rows need the mask.
-      const int lim_row = lim_all - (k0 + t * T);  // visible keys of this tile for this row
-      const int lim = lim_row - g * 32;            // ... among this warp's 32 keys
-      const bool full = lim >= 32;
-      float my_mx;
-      {
-        float mx[8];
+      // Row maxima over the visible keys of this tile (log2 domain).  Only the
+      // last tile of a split and causal rows need the mask.
+      const int tile0 = k0 + t * T;
+      const int limA = visA - tile0, limB = visB - tile0;  // visible keys of this tile
+      const bool fullA = limA >= T, fullB = limB >= T;
+      float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (full || i < lim) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        my_mx = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      }
-      float sib_mx;
-      {
-        st_shared_f32(x_max + ((buf * 2 + g) * 128 + r) * 4, my_mx);
-        const uint32_t xb = ptx::smem_u32(&bars.xm_full[buf][q4]);
-        ptx::mbar_arrive(xb);
-        if (!wait_all<false>(c, xb, (t >> 1) & 1)) { ok = false; break; }
-        sib_mx = ld_shared_f32(x_max + ((buf * 2 + (g ^ 1)) * 128 + r) * 4);
-      }
-      const float mt = lim_row > 0 ? fmaxf(my_mx, sib_mx) * c2 : -INFINITY;
-      const bool need = mt > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {  // the same decision in both siblings
-        const float m_new = need ? fmaxf(m_run, mt) : m_run;
-        const float alpha = exp2f(m_run - m_new);
+        for (int e = 0; e < 2; ++e) {
+          const int k = 8 * j + 2 * cq + e;
+          if (fullA || k < limA) mxA = fmaxf(mxA, s[4 * j + e]);
+          if (fullB || k < limB) mxB = fmaxf(mxB, s[4 * j + 2 + e]);
+        }
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+      const float mtA = limA > 0 ? mxA * c2 : -INFINITY;
+      const float mtB = limB > 0 ? mxB * c2 : -INFINITY;
+      const bool needA = mtA > mA + kRescaleThreshold, needB = mtB > mB + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, needA || needB)) {
+        const float nA = needA ? fmaxf(mA, mtA) : mA, nB = needB ? fmaxf(mB, mtB) : mB;
+        const float alA = exp2f(mA - nA), alB = exp2f(mB - nB);
         if (t > 0) {
-          // This warp's half of the CTA's O columns; the PV of the previous
-          // tile must have finished accumulating.
+          // This warp's rows of the CTA's O half; the PV of the previous tile
+          // must have finished accumulating.
           if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
             uint32_t o[32];
-            const uint32_t col = tmem + lanes + TM_O + g * 128 + ch * 32;
-            ptx::tmem_ld32(col, o);
+            const uint32_t col = tmem + lanes16 + TM_O + ch * 64;
+            ptx::tmem_ld16x256b_x8(col, o);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            ptx::tmem_st32(col, o);
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * ((i & 2) ? alB : alA));
+            ptx::tmem_st16x256b_x8(col, o);
           }
         }
-        l_run *= alpha;
-        m_run = m_new;
+        lA *= alA;
+        lB *= alB;
+        mA = nA;
+        mB = nB;
       }
-      // Weights p = 2^(s*c2 - m) (s now holds them); the row sum is exact.
-      const float neg_m = -m_run;
-      uint32_t pk[32];  // [0, 16): weights as 16-bit pairs; [16, 32): bf16 low-order terms
+      // Weights p = 2^(s*c2 - m) (s now holds them); the row sums are exact.
+      uint32_t pk[32];  // [0, 16): weights as 16-bit pairs (16x128b order); [16, 32): low-order terms
       {
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const float nmA = -mA, nmB = -mB;
+        float sA = 0.f, sB = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = fast_exp2(fmaf(s[2 * i], c2, neg_m));
-          float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg_m));
-          if (!full) {
-            p0 = 2 * i < lim ? p0 : 0.f;
-            p1 = 2 * i + 1 < lim ? p1 : 0.f;
+        for (int j = 0; j < 8; ++j) {
+          const int k = 8 * j + 2 * cq;
+          float a0 = fast_exp2(fmaf(s[4 * j], c2, nmA));
+          float a1 = fast_exp2(fmaf(s[4 * j + 1], c2, nmA));
+          float b0 = fast_exp2(fmaf(s[4 * j + 2], c2, nmB));
+          float b1 = fast_exp2(fmaf(s[4 * j + 3], c2, nmB));
+          if (!fullA) {
+            a0 = k < limA ? a0 : 0.f;
+            a1 = k + 1 < limA ? a1 : 0.f;
           }
-          s[2 * i] = p0;
-          s[2 * i + 1] = p1;
-          ls[i & 3] += p0 + p1;
-          pk[i] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+          if (!fullB) {
+            b0 = k < limB ? b0 : 0.f;
+            b1 = k + 1 < limB ? b1 : 0.f;
+          }
+          s[4 * j] = a0;
+          s[4 * j + 1] = a1;
+          s[4 * j + 2] = b0;
+          s[4 * j + 3] = b1;
+          sA += a0 + a1;
+          sB += b0 + b1;
+          pk[2 * j] = kFp8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+          pk[2 * j + 1] = kFp8 ? pack_f16(b0, b1) : pack_bf16(b0, b1);
         }
-        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        lA += sA;
+        lB += sB;
       }
-      // The P columns of this tile: keys 32g.. as 16-bit pairs at 16g, and
-      // (bf16) their low-order terms at 32 + 16g.  Both siblings have read
-      // their scores (the max swap came after), so neither overwrites the
-      // other's unread scores.
-      const uint32_t pcol = tmem + lanes + TM_S + buf * T;
-      ptx::tmem_st16(pcol + g * 16, pk);
+      // P columns of this tile: key pair (2m, 2m + 1) at column m; thread i
+      // holds pairs 4j + i%4, which is where the 16x128b shape writes.
+      const uint32_t pcol = tmem + lanes16 + TM_S + buf * T;
+      ptx::tmem_st16x128b_x8(pcol, pk);
       if constexpr (!kFp8) {
         // bf16 keeps 8 significant bits.  Where one key carries a sizeable
-        // share of a row's weight (more than 1/64 of this warp's row sum so
-        // far), the rounding would show in O, so the warp's rows also get a
-        // second bf16 term with what the first rounded away (P = P_hi + P_lo
-        // to ~16 bits) and the MMA warp adds a second PV for the tile.
-        // Elsewhere the rounding errors of many small weights average out.
-        // Each warp votes with one byte; a warp that votes no writes zeros as
-        // its second term, so the second PV is right whichever warps voted.
-        const float pmax = lim > 0 ? fast_exp2(fmaf(my_mx, c2, neg_m)) : 0.f;
-        const bool heavy = __any_sync(0xffffffffu, pmax * 64.f > l_run);
+        // share of a row's weight (more than 1/64 of this thread's part of the
+        // row sum so far), the rounding would show in O, so the warp's rows
+        // also get a second bf16 term with what the first rounded away (P =
+        // P_hi + P_lo to ~16 bits) and the MMA warp adds a second PV for the
+        // tile.  Elsewhere the rounding errors of many small weights average
+        // out.  Each warp votes with one byte; a warp that votes no writes
+        // zeros as its second term, so the second PV is right whichever warps
+        // voted.
+        const float pmA = limA > 0 ? fast_exp2(mtA - mA) : 0.f;
+        const float pmB = limB > 0 ? fast_exp2(mtB - mB) : 0.f;
+        const bool heavy = __any_sync(0xffffffffu, pmA * 64.f > lA || pmB * 64.f > lB);
         if (heavy) {  // warp-uniform
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float h0 = __uint_as_float(pk[i] << 16), h1 = __uint_as_float(pk[i] & 0xFFFF0000u);
-            pk[16 + i] = pack_bf16(s[2 * i] - h0, s[2 * i + 1] - h1);
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = __uint_as_float(pk[j] << 16), h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
+            const int e = (j & 1) ? 2 : 0;
+            pk[16 + j] = pack_bf16(s[4 * (j >> 1) + e] - h0, s[4 * (j >> 1) + e + 1] - h1);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[16 + i] = 0u;
+          for (int j = 0; j < 16; ++j) pk[16 + j] = 0u;
         }
-        ptx::tmem_st16(pcol + 32 + g * 16, pk + 16);
+        ptx::tmem_st16x128b_x8(pcol + 32, pk + 16);
         if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = heavy ? 1 : 0;
       }
       ptx::tmem_st_wait();
@@ -781,60 +783,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue ---
-    // Row sum = the two siblings' sums, added in the same order by both.
-    float inv = 0.f, l_tot = 0.f;
-    if (!live) ok = false;  // nothing to write
-    if (ok) {
-      const uint32_t x_l = sbase + OFF_RECV + X_L;
-      st_shared_f32(x_l + (g * 128 + r) * 4, l_run);
-      const uint32_t xb = ptx::smem_u32(&bars.xl_full[q4]);
-      ptx::mbar_arrive(xb);
-      ok = wait_all<false>(c, xb, 0);
-      if (ok) {
-        const float other = ld_shared_f32(x_l + ((g ^ 1) * 128 + r) * 4);
-        l_tot = g == 0 ? l_run + other : other + l_run;
-        inv = l_tot > 0.f ? s_kv / l_tot : 0.f;
-      }
-    }
-    // O is final once the last PV has drained.  It has a barrier of its own:
-    // a parity wait on o_done only tells the current phase from the one
-    // before it, and here o_done may be one phase short (another lane
-    // quarter still holds back the previous PV) or already complete.
-    if (ok && wait_all<false>(c, ptx::smem_u32(&bars.o_final), 0)) {
+    // Row sums over the quad, in the same order in both CTAs.
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    if (ok && live && wait_all<false>(c, ptx::smem_u32(&bars.o_final), 0)) {
+      // O is final once the last PV has drained (a barrier of its own: a
+      // parity wait on o_done only tells the current phase from the one
+      // before it, and o_done may be one phase short or already complete).
       ptx::tc_fence_after();
+      const float invA = lA > 0.f ? s_kv / lA : 0.f, invB = lB > 0.f ? s_kv / lB : 0.f;
+      const int rowA = rb * mla::kRowTile + rA, rowB = rb * mla::kRowTile + rB;
+      const bool okA = rowA < p.rows, okB = rowB < p.rows;
       const bool single = p.num_splits == 1;
-      const int dim0 = vdim0 + g * 128;  // this warp's 128 output dims
-      uint4* o_bf16 = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + dim0);
-      const size_t prow = ((size_t)b * p.num_splits + split) * p.rows + row;
-      float4* o_f32 = single ? nullptr : reinterpret_cast<float4*>(p.part_o + prow * mla::kDV + dim0);
+      const size_t pA = ((size_t)b * p.num_splits + split) * p.rows + rowA;
+      const size_t pB = ((size_t)b * p.num_splits + split) * p.rows + rowB;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t o[32];
-        ptx::tmem_ld32(tmem + lanes + TM_O + g * 128 + ch * 32, o);
+        ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_O + ch * 64, o);
         ptx::tmem_ld_wait();
-        if (!valid_row) continue;
-        if (single) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            o_bf16[ch * 4 + v] = w;
+        for (int j = 0; j < 8; ++j) {
+          const int dim = vdim0 + ch * 64 + 8 * j + 2 * cq;
+          const float a0 = __uint_as_float(o[4 * j]) * invA, a1 = __uint_as_float(o[4 * j + 1]) * invA;
+          const float b0 = __uint_as_float(o[4 * j + 2]) * invB, b1 = __uint_as_float(o[4 * j + 3]) * invB;
+          if (single) {
+            if (okA) *reinterpret_cast<uint32_t*>(p.out + ((size_t)b * p.rows + rowA) * mla::kDV + dim) = pack_bf16(a0, a1);
+            if (okB) *reinterpret_cast<uint32_t*>(p.out + ((size_t)b * p.rows + rowB) * mla::kDV + dim) = pack_bf16(b0, b1);
+          } else {
+            if (okA) *reinterpret_cast<float2*>(p.part_o + pA * mla::kDV + dim) = make_float2(a0, a1);
+            if (okB) *reinterpret_cast<float2*>(p.part_o + pB * mla::kDV + dim) = make_float2(b0, b1);
           }
-        } else {
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            o_f32[ch * 8 + v] =
-                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (valid_row && rank == 0 && g == 0) {
-        const float lse = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
-        if (single) p.lse[(size_t)b * p.rows + row] = lse;
-        else p.part_lse[prow] = lse;
+      if (rank == 0 && cq == 0) {
+        const float lseA = lA > 0.f ? (mA + log2f(lA)) * 0.6931471805599453f : -INFINITY;
+        const float lseB = lB > 0.f ? (mB + log2f(lB)) * 0.6931471805599453f : -INFINITY;
+        if (single) {
+          if (okA) p.lse[(size_t)b * p.rows + rowA] = lseA;
+          if (okB) p.lse[(size_t)b * p.rows + rowB] = lseB;
+        } else {
+          if (okA) p.part_lse[pA] = lseA;
+          if (okB) p.part_lse[pB] = lseB;
+        }
       }
     }
     ptx::tc_fence_before();
