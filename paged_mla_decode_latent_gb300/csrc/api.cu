@@ -9,7 +9,6 @@
 #include "../../include/mla_decode.h"
 #include "internal.h"
 
-int mla_launch_fwd_simt(const mla::FwdParams& p, void* stream);
 int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream);
 
 namespace {

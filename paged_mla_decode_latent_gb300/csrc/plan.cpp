@@ -36,10 +36,11 @@ int64_t align256(int64_t a) { return round_up(a, 256); }
 // Simulated time (ns) of one launch with a given chunk length.
 double simulate(const int32_t* lens, int batch, int row_blocks, int chunk, int splits,
                 int pairs, double ns_per_key, double ns_fixed, double ns_partial,
-                double ns_empty, double ns_combine) {
+                double ns_empty, double ns_combine_fixed, double ns_combine_per_unit) {
   std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
   for (int p = 0; p < pairs; ++p) free_at.push(0.0);
   double makespan = 0.0;
+  int64_t units = 0;  // (sequence, row block, split) units with keys: partials the combine reads
   // Dispatch order of the launch grid (2 x row blocks, batch, splits): the
   // row block varies fastest, the split slowest.
   for (int s = 0; s < splits; ++s) {
@@ -49,6 +50,7 @@ double simulate(const int32_t* lens, int batch, int row_blocks, int chunk, int s
         int64_t keys = std::max<int64_t>(0, std::min<int64_t>(lens[b], lo + chunk) - lo);
         double cost = keys > 0 ? ns_fixed + keys * ns_per_key + (splits > 1 ? ns_partial : 0.0)
                                : ns_empty;
+        units += keys > 0;
         double t = free_at.top();
         free_at.pop();
         t += cost;
@@ -57,7 +59,7 @@ double simulate(const int32_t* lens, int batch, int row_blocks, int chunk, int s
       }
     }
   }
-  return makespan + (splits > 1 ? ns_combine * splits : 0.0);
+  return makespan + (splits > 1 ? ns_combine_fixed + ns_combine_per_unit * units : 0.0);
 }
 
 }  // namespace
@@ -112,31 +114,36 @@ extern "C" int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int3
   const int pairs = std::max(1, num_sms / p.cluster_size);
   const double ns_per_key = 2200.0 / p.key_tile;
   const double ns_fixed = 10000.0, ns_empty = 400.0, ns_partial = 1000.0;
-  const double partial_bytes_total =
-      (double)batch * std::min(p.rows, p.row_tile * p.row_blocks) * (MLA_D_V * 4.0 + 4.0);
-  // The combine reads every split's partials once (about 5000 bytes/ns) after a
-  // launch gap; charged per split so that the simulation can add it up.
-  const double ns_combine_per_split = 1500.0 + partial_bytes_total / 5000.0;
+  // The combine reads every non-empty unit's partials once (about 5000
+  // bytes/ns) after a launch gap.
+  const double ns_combine_fixed = 3000.0;
+  const double ns_combine_per_unit = std::min(p.rows, p.row_tile) * (MLA_D_V * 4.0 + 4.0) / 5000.0;
   int best_chunk = (int)round_up(std::max(max_ctx, 1), p.key_tile);
   int best_splits = 1;
   if (max_ctx > 0) {
     double best_t = simulate(seq_lens_host, batch, p.row_blocks, best_chunk, 1, pairs, ns_per_key,
-                             ns_fixed, ns_partial, ns_empty, ns_combine_per_split);
+                             ns_fixed, ns_partial, ns_empty, ns_combine_fixed,
+                          ns_combine_per_unit);
     const int64_t max_splits =
         std::min<int64_t>(ceil_div(max_ctx, p.key_tile), mla::kMaxSplits);
+    // The best split candidate is kept only if it beats one unit per
+    // sequence clearly: the model leaves out that the pairs slow down a
+    // little when all of them run, and that short tail units fill their
+    // pipelines less well (measured: a 113 + 15 tile split of batch 64 x 8192
+    // was 10% slower than one unit per sequence).
+    const double unsplit_t = best_t;
+    double split_t = 1e300;
+    int split_chunk = best_chunk, split_n = 1;
     auto consider = [&](int chunk) {
       const int splits = (int)ceil_div(max_ctx, chunk);
       if (splits < 2 || splits > mla::kMaxSplits) return;
       double t = simulate(seq_lens_host, batch, p.row_blocks, chunk, splits, pairs, ns_per_key,
-                          ns_fixed, ns_partial, ns_empty, ns_combine_per_split);
-      // A split must promise a clear gain: the model leaves out that the
-      // pairs slow down a little when all of them run, and short tail units
-      // fill their pipelines less well (measured: a 113 + 15 tile split of
-      // batch 64 x 8192 was 10% slower than one unit per sequence).
-      if (t < best_t * 0.9) {
-        best_t = t;
-        best_chunk = chunk;
-        best_splits = splits;
+                          ns_fixed, ns_partial, ns_empty, ns_combine_fixed,
+                          ns_combine_per_unit);
+      if (t < split_t) {
+        split_t = t;
+        split_chunk = chunk;
+        split_n = splits;
       }
     };
     // Even splits of the longest context ...
@@ -156,6 +163,11 @@ extern "C" int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int3
       for (int64_t chunk = round_up(ceil_div(max_ctx, 2), p.key_tile); chunk < max_ctx;
            chunk += p.key_tile)
         consider((int)chunk);
+    if (split_t < unsplit_t * 0.9) {
+      best_t = split_t;
+      best_chunk = split_chunk;
+      best_splits = split_n;
+    }
   }
   p.chunk_len = best_chunk;
   p.num_splits = best_splits;
