@@ -108,6 +108,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before a rescale
 constexpr float kMaxSentinel = -1.0e30f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kSleepNs = 20000;  // suspend-time hint of a waiting thread
 
 struct Bars {
   uint64_t kv_full[4];    // operand stage ready (the 32 threads of its loader warp arrive)
@@ -151,9 +152,12 @@ __device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity
   const uint64_t t0 = ptx::globaltimer_ns();
   uint32_t n = 0;
   while (true) {
-    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+    // Sleep on the barrier rather than spin: waiting warps would otherwise
+    // take issue slots from the warps that share their sub-partition.
+    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity)
+                 : ptx::mbar_try_wait_sleep(bar, parity, kSleepNs))
       return true;
-    if ((++n & 63) == 0) {
+    if ((++n & 15) == 0) {
       if (*c.abort) return false;
       if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
         atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
