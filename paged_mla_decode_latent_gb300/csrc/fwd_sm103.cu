@@ -677,15 +677,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int tile0 = k0 + t * T;
       const int limA = visA - tile0, limB = visB - tile0;  // visible keys of this tile
       const bool fullA = limA >= T, fullB = limB >= T;
+      // Every key of the tile visible to every row of the warp (all tiles but
+      // a split's last, outside causal masking): the mask-free path.
+      const bool all_full = __all_sync(0xffffffffu, fullA && fullB);
       float mxA = -INFINITY, mxB = -INFINITY;
+      if (all_full) {
+        float xa[4], xb[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int k = 8 * j + 2 * cq + e;
-          if (fullA || k < limA) mxA = fmaxf(mxA, s[4 * j + e]);
-          if (fullB || k < limB) mxB = fmaxf(mxB, s[4 * j + 2 + e]);
+        for (int u = 0; u < 4; ++u) {
+          xa[u] = fmaxf(fmaxf(s[8 * u], s[8 * u + 1]), fmaxf(s[8 * u + 4], s[8 * u + 5]));
+          xb[u] = fmaxf(fmaxf(s[8 * u + 2], s[8 * u + 3]), fmaxf(s[8 * u + 6], s[8 * u + 7]));
         }
+        mxA = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+        mxB = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int k = 8 * j + 2 * cq + e;
+            if (k < limA) mxA = fmaxf(mxA, s[4 * j + e]);
+            if (k < limB) mxB = fmaxf(mxB, s[4 * j + 2 + e]);
+          }
+      }
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
       mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
@@ -723,29 +737,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       {
         const float nmA = -mA, nmB = -mB;
         float sA = 0.f, sB = 0.f;
+        if (all_full) {
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s[i] = fast_exp2(fmaf(s[i], c2, (i & 2) ? nmB : nmA));
+            ps[i & 3] += s[i];
+          }
+          sA = ps[0] + ps[1];
+          sB = ps[2] + ps[3];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int k = 8 * j + 2 * cq;
+            const float a0 = fast_exp2(fmaf(s[4 * j], c2, nmA));
+            const float a1 = fast_exp2(fmaf(s[4 * j + 1], c2, nmA));
+            const float b0 = fast_exp2(fmaf(s[4 * j + 2], c2, nmB));
+            const float b1 = fast_exp2(fmaf(s[4 * j + 3], c2, nmB));
+            s[4 * j] = k < limA ? a0 : 0.f;
+            s[4 * j + 1] = k + 1 < limA ? a1 : 0.f;
+            s[4 * j + 2] = k < limB ? b0 : 0.f;
+            s[4 * j + 3] = k + 1 < limB ? b1 : 0.f;
+            sA += s[4 * j] + s[4 * j + 1];
+            sB += s[4 * j + 2] + s[4 * j + 3];
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int k = 8 * j + 2 * cq;
-          float a0 = fast_exp2(fmaf(s[4 * j], c2, nmA));
-          float a1 = fast_exp2(fmaf(s[4 * j + 1], c2, nmA));
-          float b0 = fast_exp2(fmaf(s[4 * j + 2], c2, nmB));
-          float b1 = fast_exp2(fmaf(s[4 * j + 3], c2, nmB));
-          if (!fullA) {
-            a0 = k < limA ? a0 : 0.f;
-            a1 = k + 1 < limA ? a1 : 0.f;
-          }
-          if (!fullB) {
-            b0 = k < limB ? b0 : 0.f;
-            b1 = k + 1 < limB ? b1 : 0.f;
-          }
-          s[4 * j] = a0;
-          s[4 * j + 1] = a1;
-          s[4 * j + 2] = b0;
-          s[4 * j + 3] = b1;
-          sA += a0 + a1;
-          sB += b0 + b1;
-          pk[2 * j] = kFp8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
-          pk[2 * j + 1] = kFp8 ? pack_f16(b0, b1) : pack_bf16(b0, b1);
+          pk[2 * j] = kFp8 ? pack_f16(s[4 * j], s[4 * j + 1]) : pack_bf16(s[4 * j], s[4 * j + 1]);
+          pk[2 * j + 1] =
+              kFp8 ? pack_f16(s[4 * j + 2], s[4 * j + 3]) : pack_bf16(s[4 * j + 2], s[4 * j + 3]);
         }
         lA += sA;
         lB += sB;
