@@ -62,15 +62,27 @@ __global__ void __launch_bounds__(128) combine_kernel(mla::CombineParams p) {
   const float4* o_base =
       reinterpret_cast<const float4*>(p.part_o + ((size_t)b * S * p.rows + r) * mla::kDV) +
       threadIdx.x;
-  for (int s = 0; s < S; ++s) {
-    float w = w_s[s];
-    if (w == 0.f) continue;  // empty split: its partial row is never read
-    w *= inv;
-    float4 v = o_base[(size_t)s * p.rows * (mla::kDV / 4)];
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
+  const size_t stride = (size_t)p.rows * (mla::kDV / 4);
+  // Eight splits' partial rows in flight at a time.  An empty split's row
+  // holds anything (it was never written): its load is skipped and its
+  // weight is zero.
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float4 v[8];
+    float w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      w[u] = s < S ? w_s[s] : 0.f;
+      v[u] = w[u] != 0.f ? o_base[(size_t)s * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wu = w[u] * inv;
+      acc.x += wu * v[u].x;
+      acc.y += wu * v[u].y;
+      acc.z += wu * v[u].z;
+      acc.w += wu * v[u].w;
+    }
   }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);

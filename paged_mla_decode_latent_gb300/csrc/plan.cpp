@@ -116,7 +116,7 @@ extern "C" int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int3
   const double ns_fixed = 10000.0, ns_empty = 400.0, ns_partial = 1000.0;
   // The combine reads every non-empty unit's partials once (about 5000
   // bytes/ns) after a launch gap.
-  const double ns_combine_fixed = 3000.0;
+  const double ns_combine_fixed = 12000.0;  // measured: launch, dependency wait and the LSE pass
   const double ns_combine_per_unit = std::min(p.rows, p.row_tile) * (MLA_D_V * 4.0 + 4.0) / 5000.0;
   int best_chunk = (int)round_up(std::max(max_ctx, 1), p.key_tile);
   int best_splits = 1;
