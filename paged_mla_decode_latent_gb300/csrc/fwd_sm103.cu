@@ -22,12 +22,11 @@
 //                   stage read MN-major as V).
 //   softmax warps : eight warps of 16 whole rows each (TMEM 16-lane access
 //                   shapes; a row's keys spread over a quad of threads).
-//                   Each rounds its partial scores to 24 bits, sends the
-//                   packed block to the same warp of the partner CTA over
+//                   Each sends its partial scores, rounded to 24 bits and
+//                   packed, to the same warp of the partner CTA over
 //                   distributed shared memory (st.async counted on the
-//                   partner's mbarrier), adds the partner's block (a + b in
-//                   one CTA, b + a in the other: bit-identical sums, so both
-//                   CTAs take the same decisions), then runs the online
+//                   partner's mbarrier), adds the partner's block to its own
+//                   exact partial scores, then runs the online
 //                   softmax with a lazily rescaled running max and writes its
 //                   weights to TMEM over the consumed score columns (bf16: a
 //                   high part and, on tiles where one key carries much of a
@@ -204,16 +203,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return r;
 }
 
-// fp32 -> the same value rounded to 16 significant bits (round half away
-// from zero on the magnitude), low 8 bits zero.
-__device__ __forceinline__ uint32_t round24(float x) {
-  return (__float_as_uint(x) + 0x80u) & 0xFFFFFF00u;
-}
+// fp32 bits + half a unit of the 24-bit value: the top three bytes are the
+// value rounded to 16 significant bits (half away from zero on the magnitude).
+__device__ __forceinline__ uint32_t round_up_bits(float x) { return __float_as_uint(x) + 0x80u; }
 
-// Four values with zero low bytes -> three words (their upper three bytes).
-__device__ __forceinline__ void pack24(float a, float b, float c, float d, uint32_t* w) {
-  const uint32_t A = __float_as_uint(a), B = __float_as_uint(b), C = __float_as_uint(c),
-                 D = __float_as_uint(d);
+// Four values -> three words (the upper three bytes of each).
+__device__ __forceinline__ void pack24(uint32_t A, uint32_t B, uint32_t C, uint32_t D, uint32_t* w) {
   w[0] = __byte_perm(A, B, 0x5321);
   w[1] = __byte_perm(B, C, 0x6532);
   w[2] = __byte_perm(C, D, 0x7653);
@@ -616,10 +611,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t raw[32];
         ptx::tmem_ld16x256b_x8(scol, raw);
         ptx::tmem_ld_wait();
-        // Both CTAs round their own partial scores to 24 bits too, so that
-        // the sums are bit-identical.
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(round24(__uint_as_float(raw[i])));
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
       }
       // Swap partial-score blocks with the same warp of the partner CTA.  The
       // block of tile t goes into the partner's (single) buffer once the
@@ -635,9 +628,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int qd = 0; qd < 2; ++qd) {  // 16 scores -> 12 words -> 3 stores
           uint32_t w[12];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            pack24(s[16 * qd + 4 * k], s[16 * qd + 4 * k + 1], s[16 * qd + 4 * k + 2],
-                   s[16 * qd + 4 * k + 3], w + 3 * k);
+          for (int k = 0; k < 4; ++k)  // rounded to 24 bits: the top 3 bytes of x + 0x80
+            pack24(round_up_bits(s[16 * qd + 4 * k]), round_up_bits(s[16 * qd + 4 * k + 1]),
+                   round_up_bits(s[16 * qd + 4 * k + 2]), round_up_bits(s[16 * qd + 4 * k + 3]),
+                   w + 3 * k);
 #pragma unroll
           for (int v = 0; v < 3; ++v)
             ptx::st_async_u4(dst + (3 * qd + v) * 512, w[4 * v], w[4 * v + 1], w[4 * v + 2],
