@@ -443,11 +443,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int start = k0 + tile * T;
       return start + min(i * IPI + g, min(T, k1 - start) - 1);
     };
+    // key / page_size by a multiply and shifts: the unsigned form of
+    // Granlund and Montgomery, "Division by invariant integers using
+    // multiplication" (PLDI 1994), exact for every 32-bit key.  With
+    // l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+    // q = (t + ((n - t) >> 1)) >> (l - 1) where t = mulhi(m, n); d = 1 is n.
+    const uint32_t pdiv = (uint32_t)p.page_size;
+    const uint32_t plog = 32u - __clz(pdiv - 1u);
+    const uint32_t pmul = (uint32_t)(((1ull << 32) * ((1ull << plog) - pdiv)) / pdiv) + 1u;
+    const uint32_t pshift = plog > 0 ? plog - 1u : 0u;
+    auto page_of = [&](uint32_t key) -> uint32_t {
+      const uint32_t t = __umulhi(pmul, key);
+      return pdiv == 1u ? key : (t + ((key - t) >> 1)) >> pshift;
+    };
     int pg[NK];
     auto load_pages = [&](int tile) {
       if (tile >= n_tiles) return;
 #pragma unroll
-      for (int i = 0; i < NK; ++i) pg[i] = __ldg(&bt[key_of(tile, i) / p.page_size]);
+      for (int i = 0; i < NK; ++i) pg[i] = __ldg(&bt[page_of((uint32_t)key_of(tile, i))]);
     };
     load_pages(lw);
     for (int t = lw; t < n_tiles; t += NS) {
@@ -461,7 +474,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bad = true;
           page = 0;
         }
-        const int64_t r = page * p.page_size + key_of(t, i) % p.page_size;
+        const uint32_t key = (uint32_t)key_of(t, i);
+        const int64_t r = page * p.page_size + (int64_t)(key - page_of(key) * pdiv);
         row[i] = cache + r * (kFp8 ? mla::kDQK : mla::kDQK * 2);
       }
       if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
