@@ -62,6 +62,34 @@ def test_mixed_page_sizes_and_rows():
     check(syn.make_problem(2, 2, 128, [150, 64], 16, syn.KV_BF16, True, seed=10, name="rows256"))
 
 
+def _growing_rope(kv_dtype, factors, batch=64, heads=128, seed=21):
+    """The rope dims of tile i's keys (64 keys a tile) scaled by factors[i]:
+    each of the early tiles lifts the row maxima by about 7 nats, more than
+    the lazy-rescale threshold, so O is rescaled in several tiles while the
+    MMAs of the tiles before may still be in flight.  The value dims stay
+    N(0, 1), so the outputs keep their usual size; batch 64 fills the GPU."""
+    ctx = 64 * len(factors)
+    p = syn.make_problem(batch, 1, heads, [ctx] * batch, 1, syn.KV_BF16, False, seed=seed,
+                         name=f"growing_rope_{kv_dtype}")
+    x = syn.bf16_bits_to_f32(p.cache.reshape(-1, syn.D_QK)).copy()
+    f = np.ones(x.shape[0], np.float32)
+    for b in range(batch):
+        f[p.block_table[b, :ctx]] = np.repeat(np.asarray(factors, np.float32), 64)
+    x[:, syn.D_V:] *= f[:, None]
+    if kv_dtype == syn.KV_BF16:
+        p.cache = syn.f32_to_bf16_bits(x).reshape(p.cache.shape)
+    else:
+        scale = float(np.float32(np.abs(x).max() / syn.E4M3_MAX))
+        p.cache = syn.f32_to_e4m3((x / np.float32(scale)).reshape(-1)).reshape(p.cache.shape)
+        p.kv_dtype, p.kv_scale = kv_dtype, scale
+    return p
+
+
+@pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
+def test_rescale_while_earlier_pv_in_flight(kv_dtype):
+    check(_growing_rope(kv_dtype, [0.2, 6.0, 12.0, 18.0, 24.0, 1.0, 1.0, 1.0]))
+
+
 def test_split_count_invariance():
     p = syn.dense(2, 3000, seed=11)
     ref_o, ref_l = oracle_full(p)
@@ -150,3 +178,7 @@ def test_full_fp8_long_ctx109440_sampled():
 
 def test_full_mtp_causal_sampled():
     sampled_check(syn.mtp(16, 8, 64), n_rows=8)
+
+
+def test_full_mtp_h64_sq2_ps1_sampled():
+    sampled_check(syn.mtp(64, 2, 1), n_rows=8)
