@@ -5,8 +5,9 @@
 // is laid out), padded to the MMA M of 128.  The fp32 output accumulator of
 // 128 rows x 512 value dims would fill all 512 TMEM columns of one SM, so the
 // two CTAs split the value dims: CTA r owns value dims [256r, 256r+256) and,
-// for the score contraction, the same 256 latent dims (CTA 0 also takes the
-// 64 rope dims).  Each CTA therefore reads only its part of every latent row.
+// for the score contraction, the same 256 latent dims and half of the 64
+// rope dims (CTA r: rope dims [32r, 32r+32)), so both CTAs issue the same
+// number of MMAs.  Each CTA therefore reads only its part of every latent row.
 //
 // Per 64-key tile, in each CTA:
 //   loader warps  : three warps take turns by tile, one per
@@ -17,7 +18,7 @@
 //                   convert to f16 (fp8); each lane fences its own copies for
 //                   the tensor cores and arrives on the stage's barrier.
 //   MMA warp      : S_part = Q_part K_part^T  (tcgen05, A = Q from TMEM,
-//                   CTA 0's rope part A from shared memory), then
+//                   the rope part's A from shared memory), then
 //                   O_half += P V_half        (A = P from TMEM, B = the same
 //                   stage read MN-major as V).
 //   softmax warps : eight warps of 16 whole rows each (TMEM 16-lane access
@@ -62,10 +63,10 @@ namespace {
 constexpr int T = mla::kKeyTile;       // 64 keys per tile
 constexpr int ATOM = T * 128;          // one 64-dim slab of a 16-bit stage: 64 keys x 128 B
 constexpr int ATOM8 = T * 64;          // the same slab of raw fp8 codes: 64 keys x 64 B
-constexpr int SLOTS = 5;               // slabs per stage (CTA 0: 4 value + 1 rope)
+constexpr int SLOTS = 5;               // slabs per stage: 4 value + 1 rope (half of it used)
 constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
-constexpr int QROPE = 128 * 128;       // CTA 0: rope dims of Q, 128 rows x 128 B
+constexpr int QROPE = 128 * 128;       // rope dims of Q, 128 rows x 128 B
 // Exchange with the partner CTA: each softmax warp sends and receives one
 // 32-row x 32-key block of partial scores per tile, each score rounded to
 // 24 bits (16 significant bits) and packed four to three words.
@@ -352,9 +353,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, kmajor_desc(st + a * ATOM + kk * 32),
                         id_qk, (a | kk) != 0);
-        if (rank == 0) {
+        {  // this CTA's 32 rope dims: 16-dim steps 2 rank, 2 rank + 1 of the rope slab
           const uint32_t qr = sbase + OFF_QROPE;
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 2 * (int)rank; kk < 2 * (int)rank + 2; ++kk)
             ptx::mma_ss(d, kmajor_desc(qr + kk * 32), kmajor_desc(st + 4 * ATOM + kk * 32), id_qk, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
@@ -436,7 +437,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int NK = T / IPI;              // keys per lane: 16 (bf16) or 8 (fp8)
     const int lw = warp;  // the operand stage this warp owns
     const int g = lane / LPI, sub = lane % LPI;
-    const int n_slots = rank == 0 ? 5 : 4;
+    constexpr int n_slots = SLOTS;
+    // In the rope slab a CTA copies only its 32 dims: the lanes of 16-byte
+    // pieces 4 rank .. 4 rank + 3 (bf16) or of 16-code pieces 2 rank, 2 rank + 1 (fp8).
+    const bool rope_lane = (kFp8 ? (sub >> 1) : (sub >> 2)) == (int)rank;
     const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
     const char* cache = static_cast<const char*>(p.cache);
     auto key_of = [&](int tile, int i) -> int {  // i-th key of this lane, clamped to the split
@@ -486,6 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const uint32_t dst = sbase + (kFp8 ? OFF_RAW + lw * RAW_STAGE : OFF_STAGE + s * STAGE);
       for (int sl = 0; sl < n_slots; ++sl) {
+        if (sl == 4 && !rope_lane) continue;
         const int dim = sl < 4 ? vdim0 + sl * 64 : 512;
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
@@ -507,6 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         const uint32_t out = sbase + OFF_STAGE + s * STAGE;
         for (int sl = 0; sl < n_slots; ++sl) {
+          if (sl == 4 && !rope_lane) continue;
 #pragma unroll
           for (int i = 0; i < NK; ++i) {
             const int kk = i * IPI + g;
@@ -558,7 +564,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // Q (this CTA's 256 latent dims) -> TMEM as 16-bit pairs: thread i of
     // the two warps of a lane quarter writes row 32 q4 + i, two 64-dim chunks
-    // each; on CTA 0 the second warp also puts the 64 rope dims into shared
+    // each; in both CTAs the second warp also puts the 64 rope dims into shared
     // memory (128B-swizzled K-major).
     {
       const int r = q4 * 32 + lane;
@@ -580,7 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::tmem_st32(tmem + lanes + TM_Q + chunk * 32, buf);
       }
-      if (rank == 0 && g == 1) {
+      if (g == 1) {
         uint8_t* qr = smem + OFF_QROPE + r * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
