@@ -13,7 +13,8 @@
 //   loader warps  : three warps take turns by tile, one per
 //                   operand stage: block-table lookup, then
 //                   16-byte cp.async of the tile's rows in 128-byte pieces
-//                   (one 64-dim slab of one key) straight into a 128B-swizzled
+//                   (one 64-dim slab of one key; of the rope slab, the CTA's
+//                   64-byte half) straight into a 128B-swizzled
 //                   K-major stage (bf16), or into a raw stage the same lanes
 //                   convert to f16 (fp8); each lane fences its own copies for
 //                   the tensor cores and arrives on the stage's barrier.
@@ -64,7 +65,7 @@ constexpr int T = mla::kKeyTile;       // 64 keys per tile
 constexpr int ATOM = T * 128;          // one 64-dim slab of a 16-bit stage: 64 keys x 128 B
 constexpr int ATOM8 = T * 64;          // the same slab of raw fp8 codes: 64 keys x 64 B
 constexpr int SLOTS = 5;               // slabs per stage: 4 value + 1 rope (half of it used)
-constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands
+constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands (36 KB of it filled)
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // rope dims of Q, 128 rows x 128 B
 // Exchange with the partner CTA: each softmax warp sends and receives one
