@@ -68,9 +68,9 @@ constexpr int SLOTS = 5;               // slabs per stage: 4 value + 1 rope (hal
 constexpr int STAGE = SLOTS * ATOM;    // 40 KB of 16-bit operands (36 KB of it filled)
 constexpr int RAW_STAGE = SLOTS * ATOM8;  // 20 KB of fp8 codes
 constexpr int QROPE = 128 * 128;       // rope dims of Q, 128 rows x 128 B
-// Exchange with the partner CTA: each softmax warp sends and receives one
-// 32-row x 32-key block of partial scores per tile, each score rounded to
-// 24 bits (16 significant bits) and packed four to three words.
+// Exchange with the partner CTA: each softmax warp sends and receives the
+// partial scores of its 16 rows x 64 keys per tile (1024 scores), each
+// rounded to 24 bits (16 significant bits) and packed four to three words.
 constexpr int kSoftmaxWarps = 8;
 constexpr int RECV_W = 32 * 32 * 3;                  // one warp's block (3 KB)
 constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (24 KB), one buffer
@@ -424,10 +424,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ loader ---
     // Gather of a tile's cache rows with 16-byte cp.async (L2 only).  The
     // operand layout keeps a key's 64-dim slab contiguous only over 128 B, so
-    // every copy is a 128-byte piece of one row: 8 lanes per (key, slab)
-    // piece for bf16, written straight into the 128B-swizzled stage; 4 lanes
-    // per 64-byte piece of fp8 codes, written into the warp's raw stage and
-    // converted to f16 by the same lanes.  Loader warp w
+    // every copy is a 128-byte piece of one row (of the rope slab, the CTA's
+    // 64-byte half): 8 lanes per (key, slab) piece for bf16, written straight
+    // into the 128B-swizzled stage; 4 lanes per 64-byte piece of fp8 codes,
+    // written into the warp's raw stage and converted to f16 by the same
+    // lanes.  Loader warp w
     // owns operand stage w and copies tiles w, w+NS, ...: it issues a tile,
     // waits for its own copies, fences them for the tensor cores' async proxy
     // and arrives on the stage's full barrier, while the other loader warps
@@ -730,7 +731,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float alA = exp2f(mA - nA), alB = exp2f(mB - nB);
         if (t > 0) {
           // This warp's rows of the CTA's O half; the PV of the previous tile
-          // must have finished accumulating.
+          // must have finished accumulating.  One parity wait on o_done is
+          // enough: QK^T of this tile was issued after PV of tile t - 2 and
+          // the pipe runs in order, so that PV has finished and o_done is at
+          // most one phase short.  (A deeper score ring breaks this.)
           if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
