@@ -360,6 +360,32 @@ def run_gpu(args):
         except Exception:
             pass
 
+    # the same step captured once as a CUDA graph (fwd + combine) and replayed
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream()
+            mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
+                    out, lse, ws, cap)
+            mla.combine(plan, t["lens"], out, lse, ws, cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gsec = reduce_max(g0.elapsed_time(g1) / 1e3, dev)
+        graph = {"us_per_call": gsec / steps * 1e6,
+                 "value": aggregate_rate(alg["kv_bytes"] * steps, world, gsec) / 1e12,
+                 "unit": UNIT, "steps": steps}
+        st = mla.check(plan, ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st:#x} after the graph replays")
+
     # end to end through the public API with host buffers: H2D of q, block
     # table and lengths from pinned memory, decode, D2H of out and lse
     e2e = None if args.no_e2e else e2e_measure(mla, p, t, plan, ws, stream, dev,
@@ -374,6 +400,7 @@ def run_gpu(args):
         "config": dict(config_of(p, args.workload), splits=plan.num_splits,
                        chunk_len=plan.chunk_len, num_sms=plan.num_sms),
         "roofline": roof, "clocks": clk, "e2e": e2e,
+        **({"cuda_graph": graph} if graph is not None else {}),
         "gpu_launches": steps * launches_per_step,
         "context": {"mi355x_hk_m16x8_us": MI355X_HK_US.get(args.workload),
                     "note": "the pages' MI355X time for this shape (fp8 kernels, other hardware)"},
@@ -497,6 +524,8 @@ def main(argv=None):
     ap.add_argument("--ctx", type=int, default=0, help="dense workload: context (default 8192)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured as one CUDA graph and replayed")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         if args.steps <= 0:

@@ -103,6 +103,37 @@ def test_split_count_invariance():
         assert_close(o, l, outs[0][1], outs[0][2], "split vs split")
 
 
+@pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
+def test_cuda_graph_replay_matches_eager(kv_dtype):
+    """fwd + combine captured into one CUDA graph (the combine's programmatic
+    dependent launch included) and replayed give the eager bits."""
+    import torch
+    p = syn.make_problem(3, 2, 64, [3000, 700, 1], 16, kv_dtype, True, seed=18, name="graph")
+    t = to_device(p)
+    plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal, 148)
+    assert plan.num_splits > 1  # the combine is part of the graph
+    ws = mla.workspace_for(plan)
+    eager_o, eager_l, _, status = run_gpu(p, t=t, plan=plan, workspace=ws)
+    assert status == 0
+    out = torch.full((p.batch, p.sq, p.heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.batch, p.sq, p.heads), float("nan"), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream()
+        mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale, out, lse,
+                ws, s)
+        mla.combine(plan, t["lens"], out, lse, ws, s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert mla.check(plan, ws) == 0
+        assert np.array_equal(out.double().cpu().numpy(), eager_o)
+        assert np.array_equal(lse.double().cpu().numpy(), eager_l)
+    ref_o, ref_l = oracle_full(p)
+    assert_close(eager_o, eager_l, ref_o, ref_l, "graph")
+
+
 def test_empty_and_short_contexts():
     p = syn.make_problem(4, 1, 128, [0, 70, 1, 0], 1, syn.KV_BF16, False, seed=12, name="empty")
     check(p)
