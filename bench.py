@@ -351,6 +351,9 @@ def run_gpu(args):
             "kernel": "mla_decode_fwd", "roofline_us": max(t_hbm, t_tc) * 1e6,
             "alg_bytes_per_launch": alg["bytes"], "alg_flops_per_launch": alg["flops"],
             "fwd_us_mean": fwd_mean_ms * 1e3, "fwd_us_median": statistics.median(fwd_ms) * 1e3}
+    if bound == "tensor":  # the same against the tensor rate sustained over seconds
+        roof["peak_sustained"] = tc_sus
+        roof["frac_sustained"] = achieved / tc_sus
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
         try:

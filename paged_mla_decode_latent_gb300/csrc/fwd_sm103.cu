@@ -799,11 +799,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::tmem_st16x128b_x8(pcol, pk);
       if constexpr (!kFp8) {
         // bf16 keeps 8 significant bits.  Where one key carries a sizeable
-        // share of a row's weight (more than 1/64 of the row sum so far), the
+        // share of a row's weight (more than 1/16 of the row sum so far), the
         // rounding would show in O, so the warp's rows also get a second bf16
         // term with what the first rounded away (P = P_hi + P_lo to ~16 bits)
-        // and the MMA warp adds a second PV for the tile.  Elsewhere the
-        // rounding errors of many small weights average out.  Each warp votes
+        // and the MMA warp adds a second PV for the tile.  Below that share a
+        // key's rounding moves O by at most 2^-9 / 16 of its value (5e-3 for
+        // a value of 40), and the rounding errors of many small weights
+        // average out.  Each warp votes
         // with one byte; a warp that votes no writes zeros as its second
         // term, so the second PV is right whichever warps voted.
         const float pmA = limA > 0 ? fast_exp2(mtA - mA) : 0.f;
@@ -812,7 +814,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float rsB = lB + __shfl_xor_sync(0xffffffffu, lB, 1);
         rsA += __shfl_xor_sync(0xffffffffu, rsA, 2);
         rsB += __shfl_xor_sync(0xffffffffu, rsB, 2);
-        const bool heavy = __any_sync(0xffffffffu, pmA * 64.f > rsA || pmB * 64.f > rsB);
+        const bool heavy = __any_sync(0xffffffffu, pmA * 16.f > rsA || pmB * 16.f > rsB);
         if (heavy) {  // warp-uniform
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
