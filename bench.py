@@ -53,7 +53,7 @@ def make_workload(name: str, seed: int = 0, batch: int = 0, ctx: int = 0) -> syn
     if name == "ragged_fp8":
         return syn.ragged(syn.KV_FP8_E4M3, seed=seed)
     if name == "fp8_long":
-        return syn.fp8_long(109440, seed=seed)
+        return syn.fp8_long(ctx or 109440, seed=seed)
     if name == "mtp":
         return syn.mtp(64, 2, 1, seed=seed)
     raise ValueError(name)
@@ -524,7 +524,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="dense",
                     choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp"])
     ap.add_argument("--batch", type=int, default=0, help="dense workload: batch (default 64)")
-    ap.add_argument("--ctx", type=int, default=0, help="dense workload: context (default 8192)")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="dense (default 8192) or fp8_long (default 109440) workload: context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--graph", action="store_true",
