@@ -94,11 +94,11 @@ def test_split_count_invariance():
     p = syn.dense(2, 3000, seed=11)
     ref_o, ref_l = oracle_full(p)
     outs = []
-    for num_sms in (2, 148, 4000):
+    for num_sms in (2, 8, 16, 148, 4000):  # 1, 2, 4 and 24 splits
         out, lse, plan, _ = run_gpu(p, num_sms=num_sms)
         assert_close(out, lse, ref_o, ref_l, f"num_sms={num_sms} splits={plan.num_splits}")
         outs.append((plan.num_splits, out, lse))
-    assert len({s for s, _, _ in outs}) >= 2
+    assert len({s for s, _, _ in outs}) >= 3
     for _, o, l in outs[1:]:
         assert_close(o, l, outs[0][1], outs[0][2], "split vs split")
 
@@ -132,6 +132,17 @@ def test_cuda_graph_replay_matches_eager(kv_dtype):
         assert np.array_equal(lse.double().cpu().numpy(), eager_l)
     ref_o, ref_l = oracle_full(p)
     assert_close(eager_o, eager_l, ref_o, ref_l, "graph")
+
+
+@pytest.mark.parametrize("num_sms", [16, 148])
+def test_splits_two_row_blocks_empty_sequence(num_sms):
+    # 256 rows (two row blocks per sequence), causal, an empty sequence and one
+    # shorter than a split, over 3 and 4 splits
+    p = syn.make_problem(3, 2, 128, [700, 40, 0], 16, syn.KV_BF16, True, seed=19, name="splits")
+    out, lse, plan, status = run_gpu(p, num_sms=num_sms)
+    assert plan.num_splits in (3, 4) and status == 0
+    ref_o, ref_l = oracle_full(p)
+    assert_close(out, lse, ref_o, ref_l, f"splits={plan.num_splits}")
 
 
 def test_empty_and_short_contexts():
