@@ -7,6 +7,9 @@ splits) over the whole batch, with every input already resident in HBM.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload dense|ragged_bf16|ragged_fp8|fp8_long|mtp]
 
+With --gpus N > 1 outside torchrun the script starts the N ranks itself
+(torch.distributed.run, 127.0.0.1); under torchrun WORLD_SIZE must equal N.
+
 Prints ONE JSON line (rank 0).  ``value`` is the whole-job KV-cache read rate
 in TB/s (KV bytes of all ranks / max-over-ranks time); the per-call latency is
 in ``us_per_call``.  Under torchrun (N > 1) every rank runs an independent
@@ -515,9 +518,46 @@ def kernel_revision() -> str:
     return h.hexdigest()[:12]
 
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def launch_replicas(n: int, argv) -> int:
+    """Start one rank per GPU (torch.distributed.run on 127.0.0.1) running
+    this script with the same arguments; returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(_free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def run_launch_check(args):
+    """The replica launch and the cross-rank reduction alone, on CPU ranks
+    (gloo): no decode runs.  Rank 0 prints what every rank saw."""
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    dist.init_process_group("gloo")
+    t = reduce_max(1.0 + 0.5 * rank)
+    seen = [None] * world
+    dist.all_gather_object(seen, {"rank": rank, "world": world, "max_s": t,
+                                  "rate": aggregate_rate(1000.0, world, t)})
+    if rank == 0:
+        print(json.dumps({"launch_check": {"gpus": args.gpus, "world": world, "ranks": seen}}))
+    dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="replicas, one per GPU; started here through torch.distributed.run "
+                         "unless already launched that way with WORLD_SIZE == N")
+    ap.add_argument("--launch-check", action="store_true",
+                    help="only start the ranks and check the cross-rank reduction (CPU, gloo)")
     ap.add_argument("--steps", type=int, default=0, help="0 = enough for ~2.5 s of timed work")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -531,6 +571,14 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured as one CUDA graph and replayed")
     args = ap.parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and "RANK" not in os.environ:
+        return launch_replicas(args.gpus, argv)
+    if args.gpus != world:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: launch one rank "
+                         "per GPU with --nproc-per-node equal to --gpus")
+    if args.launch_check:
+        return run_launch_check(args)
     if args.impl == "reference":
         if args.steps <= 0:
             args.steps = 3

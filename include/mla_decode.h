@@ -80,7 +80,8 @@ typedef enum mla_kv_dtype {
 
 /* Bits of the device status word (OR-ed together by the kernels). */
 #define MLA_DEVFLAG_BAD_PAGE 0x1   /* block-table entry outside [0, num_pages) */
-#define MLA_DEVFLAG_CTX_RANGE 0x2  /* seq_lens[b] beyond the plan's max_ctx  */
+#define MLA_DEVFLAG_CTX_RANGE 0x2  /* seq_lens[b] < 0 or beyond the plan's max_ctx
+                                      (clamped to [0, max_ctx] on the device) */
 #define MLA_DEVFLAG_TIMEOUT 0x4    /* a bounded barrier wait gave up         */
 #define MLA_DEVFLAG_Q_RANGE 0x8    /* fp8 path: |q| beyond the fp16 range    */
 
@@ -112,7 +113,10 @@ typedef struct mla_decode_plan_t {
   int32_t cluster_size; /* CTAs cooperating on one (b, row block, split) */
   int32_t grid_x, grid_y, grid_z; /* launch grid of mla_decode_fwd: (2 x row_blocks, batch,
                                      num_splits); splits vary slowest */
-  int32_t reserved0;
+  int32_t wait_limit_us; /* bound of every device-side wait, in microseconds; 0 (what
+                            mla_decode_plan writes) means 2 s.  The one field a caller
+                            may change: a short limit is how the timeout path is
+                            exercised (waits then give up, MLA_ERR_TIMEOUT) */
   int64_t ws_partial_o_offset;   /* byte offset of fp32 [B, S, rows, 512] partials */
   int64_t ws_partial_lse_offset; /* byte offset of fp32 [B, S, rows] partial LSEs */
   int64_t ws_status_offset;      /* byte offset of the int32 device status word */

@@ -49,7 +49,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "batch", "num_heads", "sq", "page_size", "kv_dtype", "causal", "rows",
         "row_tile", "row_blocks", "max_ctx", "key_tile", "chunk_len", "num_splits", "num_sms",
-        "cluster_size", "grid_x", "grid_y", "grid_z", "reserved0")] + [
+        "cluster_size", "grid_x", "grid_y", "grid_z", "wait_limit_us")] + [
         (n, ctypes.c_int64) for n in (
             "ws_partial_o_offset", "ws_partial_lse_offset", "ws_status_offset", "workspace_bytes")]
 

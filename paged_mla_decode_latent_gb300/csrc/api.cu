@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/mla_decode.h"
 #include "internal.h"
@@ -12,6 +13,8 @@
 int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream);
 
 namespace {
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -23,6 +26,7 @@ int check_plan(const mla_decode_plan_t* plan) {
     return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype != MLA_KV_BF16 && plan->kv_dtype != MLA_KV_FP8_E4M3)
     return MLA_ERR_INVALID_ARG;
+  if (plan->wait_limit_us < 0) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 
@@ -68,6 +72,8 @@ extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, cons
   p.part_lse =
       plan->num_splits > 1 ? reinterpret_cast<float*>(ws + plan->ws_partial_lse_offset) : nullptr;
   p.status = reinterpret_cast<int32_t*>(ws + plan->ws_status_offset);
+  p.wait_ns = plan->wait_limit_us > 0 ? (uint64_t)plan->wait_limit_us * 1000ull
+                                      : kDefaultWaitNs;
   p.batch = plan->batch;
   p.heads = plan->num_heads;
   p.sq = plan->sq;
@@ -125,6 +131,23 @@ extern "C" int mla_decode_check(const mla_decode_plan_t* plan, const void* works
   if (v != 0) return MLA_ERR_DEVICE_CHECK;
   return MLA_OK;
 }
+
+namespace mla {
+
+cudaError_t opt_in_smem(const void* kernel, int bytes, int dev, int slot) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static uint32_t done[kMaxDev] = {};
+  if (dev < 0 || dev >= kMaxDev || slot < 0 || slot >= 32)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev] & (1u << slot)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] |= 1u << slot;
+  return e;
+}
+
+}  // namespace mla
 
 int mla_launch_fwd(const mla::FwdParams& p, void* stream) {
   return mla_launch_fwd_sm103(p, stream);

@@ -45,9 +45,11 @@
 // head group, KV chunk) with chunks past a sequence's end returning at once
 // ("perf(mla): chunk the non-FP4 gather_kv_b_proj over KV", description).
 //
-// Every wait is bounded (about 2 s of wall time).  A wait that runs out sets
-// MLA_DEVFLAG_TIMEOUT in the status word and the CTA winds down instead of
-// hanging the GPU.
+// Every wait is bounded (2 s of wall time unless the plan sets another
+// limit).  A wait that runs out sets MLA_DEVFLAG_TIMEOUT in the status word
+// and the CTA winds down instead of hanging the GPU: it stops issuing, drains
+// its copies and MMAs, frees TMEM and meets its partner at the final cluster
+// barrier (the partner's own waits run out in turn).
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -111,7 +113,7 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before a rescale
 constexpr float kMaxSentinel = -1.0e30f;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 500000000ull;  // bound of the wind-down waits after an abort
 constexpr uint32_t kSleepNs = 20000;  // suspend-time hint of a waiting thread
 
 struct Bars {
@@ -134,6 +136,7 @@ static_assert(sizeof(Bars) <= 512, "barrier block");
 struct Ctx {
   int32_t* status;
   volatile int32_t* abort;
+  uint64_t limit_ns;  // bound of every pipeline wait (FwdParams::wait_ns)
 };
 
 // Wait used only while winding down after an abort: ignores the abort word,
@@ -141,7 +144,7 @@ struct Ctx {
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kTimeoutNs / 4) return false;
+    if (ptx::globaltimer_ns() - t0 > kDrainNs) return false;
   }
   return true;
 }
@@ -149,34 +152,28 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 // Bounded wait on an mbarrier phase.  Returns false (and flags the status
 // word and the CTA's abort word) if the phase did not complete in time or
 // another warp of this CTA already gave up.
-template <bool kCluster>
 __device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity) {
-  if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
-    return true;
+  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
-  uint32_t n = 0;
   while (true) {
     // Sleep on the barrier rather than spin: waiting warps would otherwise
-    // take issue slots from the warps that share their sub-partition.
-    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity)
-                 : ptx::mbar_try_wait_sleep(bar, parity, kSleepNs))
-      return true;
-    if ((++n & 15) == 0) {
-      if (*c.abort) return false;
-      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
-        atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
-        *c.abort = 1;
-        return false;
-      }
+    // take issue slots from the warps that share their sub-partition.  A
+    // failed try suspends the thread for up to kSleepNs, so reading the
+    // timer after each one costs nothing that matters.
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (*c.abort) return false;
+    if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
+      atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
+      *c.abort = 1;
+      return false;
     }
   }
 }
 
 // The same, decided for the whole warp: true only if every lane's wait
 // succeeded, so warp-collective tcgen05 instructions stay convergent.
-template <bool kCluster>
 __device__ __forceinline__ bool wait_all(const Ctx& c, uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, wait<kCluster>(c, bar, parity));
+  return __all_sync(0xffffffffu, wait(c, bar, parity));
 }
 
 // 2^x with the SFU's approximate exp2 (inputs below -126 flush to +0, -inf
@@ -280,11 +277,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int rb = blockIdx.x >> 1, b = blockIdx.y, split = blockIdx.z;
 
+  // A context the plan does not cover is clamped to [0, max_ctx] and
+  // flagged.  max_ctx keys fit the block table (bt_stride * page_size >=
+  // max_ctx is checked on the host) and the splits (num_splits * chunk_len
+  // >= max_ctx), so no table entry past the sequence's row is read.
   int ctx = p.seq_lens[b];
-  const int covered = p.num_splits * p.chunk_len;
-  if (ctx < 0 || ctx > covered) {
-    if (threadIdx.x == 0 && rank == 0) atomicOr(p.status, MLA_DEVFLAG_CTX_RANGE);
-    ctx = ctx < 0 ? 0 : covered;
+  if (ctx < 0 || ctx > p.max_ctx) {
+    if (threadIdx.x == 0 && rank == 0 && split == 0) atomicOr(p.status, MLA_DEVFLAG_CTX_RANGE);
+    ctx = ctx < 0 ? 0 : p.max_ctx;
   }
   const int k0 = split * p.chunk_len;
   const int k1 = min(k0 + p.chunk_len, ctx);
@@ -337,14 +337,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  Ctx c{p.status, &bars.abort};
+  Ctx c{p.status, &bars.abort, p.wait_ns};
 
   if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
       const uint32_t id_qk = ptx::idesc_f16(128, T, kAB, false, false);
       const uint32_t id_pv = ptx::idesc_f16(128, 256, kAB, false, true);
-      bool ok = wait<false>(c, ptx::smem_u32(&bars.q_ready), 0);
+      bool ok = wait(c, ptx::smem_u32(&bars.q_ready), 0);
       ptx::tc_fence_after();
       auto issue_qk = [&](int u) {
         const int s = u % NS;
@@ -410,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t now = ptx::globaltimer_ns();
           if (t_last == 0) t_last = now;
           if (*c.abort) ok = false;
-          else if (now - t_last > kTimeoutNs) {
+          else if (now - t_last > c.limit_ns) {
             atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
             *c.abort = 1;
             ok = false;
@@ -487,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
       load_pages(t + NS);
       if constexpr (!kFp8) {
-        if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
+        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
           break;
       }
       const uint32_t dst = sbase + (kFp8 ? OFF_RAW + lw * RAW_STAGE : OFF_STAGE + s * STAGE);
@@ -510,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if constexpr (kFp8) {
         // e4m3 codes -> f16 operands (exact); the per-tensor scale is applied
         // to the scores and the output instead.
-        if (t >= NS && !wait_all<false>(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
+        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1))
           break;
         const uint32_t out = sbase + OFF_STAGE + s * STAGE;
         for (int sl = 0; sl < n_slots; ++sl) {
@@ -620,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
-      if (!wait_all<false>(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
+      if (!wait_all(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
       if (!live) {
         if (!kFp8 && lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = 0;
         ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[buf]));
@@ -641,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // partner has read tile t - 1 from it.
       if (t >= 1) {
         if (lane == 0) ptx::mbar_arrive_expect_tx(recv_free, 4);
-        if (!wait_all<false>(c, recv_free, (t - 1) & 1)) { ok = false; break; }
+        if (!wait_all(c, recv_free, (t - 1) & 1)) { ok = false; break; }
       }
       {
         const uint32_t dst = peer_recv + lane * 16;
@@ -662,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       {
         if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
-        if (!wait_all<false>(c, recv_full, t & 1)) { ok = false; break; }
+        if (!wait_all(c, recv_full, t & 1)) { ok = false; break; }
         const uint32_t src = my_recv + lane * 16;
         uint32_t fold = 0;
 #pragma unroll
@@ -735,7 +735,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // enough: QK^T of this tile was issued after PV of tile t - 2 and
           // the pipe runs in order, so that PV has finished and o_done is at
           // most one phase short.  (A deeper score ring breaks this.)
-          if (!wait_all<false>(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
+          if (!wait_all(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
@@ -840,7 +840,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    if (ok && live && wait_all<false>(c, ptx::smem_u32(&bars.o_final), 0)) {
+    if (ok && live && wait_all(c, ptx::smem_u32(&bars.o_final), 0)) {
       // O is final once the last PV has drained (a barrier of its own: a
       // parity wait on o_done only tells the current phase from the one
       // before it, and o_done may be one phase short or already complete).
@@ -908,12 +908,11 @@ int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
   const bool fp8 = p.kv_dtype == MLA_KV_FP8_E4M3;
   auto kernel = fp8 ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
   const int smem = fp8 ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[fp8]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
-    attr_done[fp8] = true;
-  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, fp8 ? 1 : 0);
+  if (e != cudaSuccess) return (int)e;
   // Splits vary slowest, so every sequence's first chunk is dispatched
   // before any second chunk (the planner simulates this order).
   dim3 grid(p.row_blocks * 2, p.batch, p.num_splits);

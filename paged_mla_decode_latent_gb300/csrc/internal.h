@@ -2,6 +2,8 @@
 // translation units (not part of the public ABI).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 namespace mla {
@@ -30,9 +32,15 @@ struct FwdParams {
   float* part_o;            // fp32 [B, S, rows, 512] (S > 1)
   float* part_lse;          // fp32 [B, S, rows]      (S > 1)
   int32_t* status;          // device status word
+  uint64_t wait_ns;         // bound of every pipeline wait inside the kernel
   int batch, heads, sq, rows, page_size, kv_dtype, causal;
   int chunk_len, num_splits, max_ctx, row_blocks;
 };
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on device `dev`,
+// once per (device, kernel slot); thread-safe.  Slots name the library's
+// kernels that need more than 48 KB (at most 32 of them).
+cudaError_t opt_in_smem(const void* kernel, int bytes, int dev, int slot);
 
 struct CombineParams {
   const float* part_o;

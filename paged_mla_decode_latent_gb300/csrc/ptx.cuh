@@ -1,6 +1,6 @@
-// ptx.cuh -- hand-written inline-PTX wrappers for sm_103a: mbarrier, TMA
-// (cp.async.bulk.tensor), tcgen05 (TMEM alloc / MMA / commit / ld / st),
-// cluster shared memory and programmatic dependent launch.  Written from the
+// ptx.cuh -- hand-written inline-PTX wrappers for sm_103a: mbarrier,
+// cp.async, tcgen05 (TMEM alloc / MMA / commit / ld / st) and stores into
+// the shared memory of another CTA of the cluster.  Written from the
 // PTX ISA's descriptions of these instructions; no library code is used.
 #pragma once
 
@@ -53,12 +53,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -99,45 +93,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Acquire at cluster scope: makes a remote CTA's writes (released by its
-// remote arrive) visible to this thread.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// ------------------------------------------------------------------- TMA ---
-
-__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
-// 2-D tiled load of box {c0 (inner), c1} into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
-// Four rows r0..r3 (any order) of width box[0] starting at column c0.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t c0, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
+// ------------------------------------------------------------- cp.async ---
 
 // 16-byte global -> shared copy through L2 only (cp.async.cg), in the
 // current commit group of the issuing thread.
@@ -294,24 +250,6 @@ __device__ __forceinline__ void tmem_st16x128b_x8(uint32_t taddr, const uint32_t
       : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
-// 32 lanes x 64 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
-      : "memory");
-}
-
 // Instruction descriptor of kind::f16 with fp32 accumulation.
 //   ab_type: 0 = f16, 1 = bf16;  *_mn: operand is MN-major (else K-major)
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, uint32_t ab_type, bool a_mn,
@@ -335,24 +273,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // ------------------------------------------------- cluster shared memory ---
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c,
-                                              float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-// Asynchronous 16-byte store into another CTA's shared memory that counts
-// its bytes on an mbarrier of that CTA (complete_tx); needs no fence.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
-                                            float d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
                                              uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
@@ -374,13 +294,5 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-
-// ------------------------------------------------------------------- PDL ---
-
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace ptx

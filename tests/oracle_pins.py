@@ -223,6 +223,71 @@ def pin_matches_torch_sdpa(orc):
     assert np.allclose(out[0].reshape(sq * h, 512), ref, rtol=1e-12, atol=1e-13)
 
 
+def _pool_layout(seqs, ps, seed):
+    """Place each sequence's logical key rows (list of [n_b, 576] arrays) into
+    pages of size ps drawn from one shuffled pool.  Returns (cache, block_table,
+    seq_lens); the rows are known, so expected values need no gather."""
+    nblk = [max(1, -(-r.shape[0] // ps)) for r in seqs]
+    total = sum(nblk)
+    perm = np.random.default_rng(seed).permutation(total).astype(np.int32)
+    cache = np.zeros((total, ps, 576), np.uint16)
+    bt = np.zeros((len(seqs), max(nblk)), np.int32)
+    off = 0
+    for b, rows in enumerate(seqs):
+        for k in range(nblk[b]):
+            page = perm[off + k]
+            bt[b, k] = page
+            chunk = rows[k * ps:(k + 1) * ps]
+            cache[page, :chunk.shape[0]] = chunk
+        off += nblk[b]
+    return cache, bt, np.array([r.shape[0] for r in seqs], np.int32)
+
+
+def pin_decode_row_matches_sdpa_causal(orc):
+    """decode_row on every (b, i, h) of a causal MTP batch (three sequences,
+    Sq = 4, 3 heads, page size 16, shuffled pages, one sequence shorter than
+    Sq) against torch's fp64 scaled_dot_product_attention of that query row
+    over the logical rows its token may see, keys [0, ctx - Sq + i + 1)."""
+    import torch
+    sq, h, lens = 4, 3, [40, 17, 3]
+    seqs = [rand_bits(30 + b, (n, 576)) for b, n in enumerate(lens)]
+    cache, bt, sl = _pool_layout(seqs, 16, seed=33)
+    q = rand_bits(34, (len(lens), sq, h, 576))
+    for b, n_ctx in enumerate(lens):
+        k = torch.from_numpy(_f(seqs[b]))
+        for i in range(sq):
+            n = max(0, min(n_ctx, n_ctx - sq + i + 1))
+            for hh in range(h):
+                out, lse = orc.decode_row(q, cache, syn.KV_BF16, 1.0, 16, bt, sl, SCALE, True,
+                                          b, i, hh)
+                if n == 0:
+                    assert np.all(out == 0) and lse == -math.inf, (b, i, hh)
+                    continue
+                qr = torch.from_numpy(_f(q[b, i, hh]))[None, None, None]
+                kk = k[:n][None, None]
+                ref = torch.nn.functional.scaled_dot_product_attention(
+                    qr, kk, kk[..., :512], scale=SCALE)[0, 0, 0].numpy()
+                z = SCALE * (_f(seqs[b][:n]) @ _f(q[b, i, hh]))
+                ref_lse = float(np.logaddexp.reduce(z))
+                assert np.allclose(out, ref, rtol=1e-12, atol=1e-13), (b, i, hh)
+                assert abs(lse - ref_lse) < 1e-12, (b, i, hh)
+
+
+def pin_decode_row_equals_decode(orc):
+    """decode_row gives, bit for bit, the row decode gives for the whole batch
+    (causal MTP, Sq = 4, page size 16, ragged contexts)."""
+    p = syn.make_problem(3, 4, 3, [53, 6, 21], 16, syn.KV_BF16, True, seed=35)
+    args = (p.q_bits, p.cache, p.kv_dtype, p.kv_scale, p.page_size, p.block_table,
+            p.seq_lens, p.softmax_scale, p.causal)
+    full_o, full_l = orc.decode(*args)
+    for b in range(p.batch):
+        for i in range(p.sq):
+            for hh in range(p.heads):
+                o, l = orc.decode_row(*args, b, i, hh)
+                assert np.array_equal(o, full_o[b, i, hh]), (b, i, hh)
+                assert l == full_l[b, i, hh] or (np.isneginf(l) and np.isneginf(full_l[b, i, hh]))
+
+
 # ------------------------------------------------------------ invariances ---
 
 def _random_problem_rows(seed, n):

@@ -2,12 +2,15 @@
 device, run the library through its C ABI, and compare with the fp64 oracle.
 
 Tolerances (bf16 output against the fp64 oracle on the same bits):
-  max (|out - ref| - ulp_bf16(ref) / 2)   <= 1.5e-2
+  |out - ref|                             <= 1.5e-2        where |ref| < 4
+  |out - ref| - ulp_bf16(ref) / 2         <= 1.5e-2        where |ref| >= 4
   ||out - ref||_F / ||ref||_F             <= 4e-3
   max |lse - ref_lse|                     <= 1e-3
-The max-abs bound is taken beyond the rounding of the exact value to bf16:
-the output format alone is off by up to half a bf16 ulp, which exceeds 1.5e-2
-once |ref| >= 4 (the MTP workload's x8 outlier rows give |out| near 30).
+The max-abs bound is the stated 1.5e-2 on every element a correctly rounded
+bf16 value can meet it on: half a bf16 ulp is at most 2^-7 = 7.8e-3 below 4.
+From |ref| = 4 up, half an ulp (1.56e-2 and more) exceeds 1.5e-2 by itself,
+so there the bound applies to the error beyond that rounding (the MTP
+workload's x8 outlier rows give |out| near 30).
 Rows with no visible key must give out == 0 and lse == -inf exactly.
 """
 from __future__ import annotations
@@ -19,6 +22,7 @@ import mla_synth as syn
 MAX_ABS = 1.5e-2
 REL_FRO = 4e-3
 LSE_ABS = 1e-3
+BIG = 4.0  # from here up half a bf16 ulp exceeds MAX_ABS
 
 
 def to_device(p: syn.Problem, device="cuda"):
@@ -80,11 +84,15 @@ def assert_close(out, lse, ref_out, ref_lse, what=""):
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     err = np.abs(o - r)
     max_abs = float(err.max())
-    beyond = float((err - bf16_half_ulp(r)).max())
+    big = np.abs(r) >= BIG
+    small_err = float(err[~big].max()) if (~big).any() else 0.0
+    beyond = float((err[big] - bf16_half_ulp(r[big])).max()) if big.any() else 0.0
     fro = float(np.linalg.norm(o - r) / max(np.linalg.norm(r), 1e-30))
     lse_err = float(np.abs(lse[ok] - ref_lse[ok]).max())
-    stats = dict(max_abs=max_abs, beyond_rounding=beyond, rel_fro=fro, lse_abs=lse_err)
-    assert beyond <= MAX_ABS, f"{what}: max abs beyond bf16 rounding {beyond:.3e} > {MAX_ABS} {stats}"
+    stats = dict(max_abs=max_abs, max_abs_below_4=small_err, beyond_rounding_from_4=beyond,
+                 n_from_4=int(big.sum()), rel_fro=fro, lse_abs=lse_err)
+    assert small_err <= MAX_ABS, f"{what}: max abs {small_err:.3e} > {MAX_ABS} where |ref| < 4 {stats}"
+    assert beyond <= MAX_ABS, f"{what}: max abs beyond bf16 rounding {beyond:.3e} > {MAX_ABS} where |ref| >= 4 {stats}"
     assert fro <= REL_FRO, f"{what}: rel Frobenius {fro:.3e} > {REL_FRO} {stats}"
     assert lse_err <= LSE_ABS, f"{what}: lse abs {lse_err:.3e} > {LSE_ABS} {stats}"
     return stats

@@ -53,3 +53,35 @@ def test_single_process_is_identity():
     import bench
     assert bench.reduce_max(3.25) == 3.25
     assert bench.aggregate_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_gpus_2_starts_two_ranks_on_cpu():
+    """bench.py --gpus 2 outside torchrun starts two ranks itself; with
+    --launch-check they only run the cross-rank reduction over gloo."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--launch-check"], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+    d = json.loads(line)["launch_check"]
+    assert d["gpus"] == 2 and d["world"] == 2
+    assert sorted(x["rank"] for x in d["ranks"]) == [0, 1]
+    for x in d["ranks"]:
+        assert x["max_s"] == pytest.approx(1.5)
+        assert x["rate"] == pytest.approx(2 * 1000.0 / 1.5)
+
+
+def test_gpus_mismatch_is_refused():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--launch-check"], capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr

@@ -54,6 +54,10 @@ MUTATIONS = [
     ("query_row_transposed", "(((int64_t)bb * Sq + i) * H + h)", "(((int64_t)bb * H + h) * Sq + i)"),
     ("bf16_wrong_half", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
     ("weights_skip_max", "double w = exp(z[j - lo] - l);", "double w = exp(z[j - lo] - m);"),
+    ("row_query_transposed", "q + (((int64_t)b * Sq + i) * H + h) * ORACLE_D_QK",
+     "q + (((int64_t)b * H + h) * Sq + i) * ORACLE_D_QK"),
+    ("row_sees_all_tokens_keys", "int64_t n = visible_keys(seq_lens[b], Sq, i, causal);",
+     "int64_t n = visible_keys(seq_lens[b], Sq, Sq - 1, causal);"),
 ]
 
 

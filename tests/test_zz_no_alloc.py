@@ -6,8 +6,10 @@ must not call cudaMalloc / cudaFree (they can synchronise the device).  They
 call mla_decode_fwd_noalloc with inputs and outputs only; the library takes
 its scratch from a fixed 64 MiB device array of its own.  This file checks,
 through the C ABI, that two calls in a row give what mla_decode_fwd +
-mla_decode_combine give with a caller-owned workspace, within the parity
-tolerance.  It is collected last on purpose.
+mla_decode_combine give with a caller-owned workspace, bit for bit (the same
+plan and kernels run; only the workspace differs), after the scratch was left
+holding another plan's partials, and that the result meets the parity
+tolerance against the oracle.  It is collected last on purpose.
 """
 import ctypes
 
@@ -16,7 +18,7 @@ import pytest
 
 import mla_synth as syn
 import paged_mla_decode_latent_gb300 as mla
-from parity import assert_close, run_gpu, to_device
+from parity import assert_close, oracle_full, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -58,9 +60,21 @@ def test_noalloc_matches_workspace_entry_point_twice(kv_dtype):
     assert plan.num_splits > 1  # the scratch holds split partials
     ref_o, ref_l, _, status = run_gpu(p, t=t, plan=plan)
     assert status == 0
+    # Leave other contents in the scratch first: a different batch and split
+    # count, so stale partials of another plan sit where this plan reads.
+    other = syn.make_problem(2, 2, 64, [5000, 900], 16, kv_dtype, True, seed=22, name="other")
+    ot = to_device(other)
+    oplan = mla.plan(other.seq_lens, other.heads, other.sq, other.page_size, other.kv_dtype,
+                     other.causal, 148)
+    assert oplan.num_splits != plan.num_splits
+    call_noalloc(other, ot, oplan)
+    # Same plan and kernels as the workspace entry point: the same bits.
     for _ in range(2):  # the scratch keeps the previous call's contents
         out, lse = call_noalloc(p, t, plan)
-        assert_close(out, lse, ref_o, ref_l, "noalloc vs workspace entry point")
+        assert np.array_equal(out, ref_o), "noalloc output differs from the workspace entry point"
+        assert np.array_equal(lse, ref_l), "noalloc lse differs from the workspace entry point"
+    ref = oracle_full(p)
+    assert_close(out, lse, *ref, "noalloc vs oracle")
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
