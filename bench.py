@@ -270,22 +270,55 @@ def run_gpu(args):
     p = make_workload(args.workload, seed=rank, batch=args.batch, ctx=args.ctx)
     alg = algorithmic(p)
     t = to_device(p, dev)
-    plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal)
-    ws = mla.workspace_for(plan, dev)
     out = torch.empty((p.batch, p.sq, p.heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((p.batch, p.sq, p.heads), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 1 + (1 if plan.num_splits > 1 else 0)
+    if args.dplan:
+        # device-planned: the partition is computed on the GPU every step
+        plan = mla.dplan_info(p.batch, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal,
+                              int(t["bt"].shape[1]) * p.page_size)
+        ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        launches_per_step = 3
+
+        def pre(s):
+            mla.plan_device(plan, t["lens"], ws, stream=s)
+
+        def fwd_call(s):
+            mla.fwd_dplan(plan, t["q"], t["cache"], t["scale"], t["bt"], p.softmax_scale, out, lse,
+                          ws, stream=s)
+
+        def post(s):
+            mla.combine_dplan(plan, out, lse, ws, stream=s)
+
+        def status():
+            return mla.dplan_check(plan, ws)
+    else:
+        plan = mla.plan(p.seq_lens, p.heads, p.sq, p.page_size, p.kv_dtype, p.causal)
+        ws = mla.workspace_for(plan, dev)
+        launches_per_step = 1 + (1 if plan.num_splits > 1 else 0)
+
+        def pre(s):
+            pass
+
+        def fwd_call(s):
+            mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
+                    out, lse, ws, s)
+
+        def post(s):
+            mla.combine(plan, t["lens"], out, lse, ws, s)
+
+        def status():
+            return mla.check(plan, ws)
 
     def step():
-        mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
-                out, lse, ws, stream)
-        mla.combine(plan, t["lens"], out, lse, ws, stream)
+        pre(stream)
+        fwd_call(stream)
+        post(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    st = mla.check(plan, ws)
+    st = status()
     if st != 0:
         raise RuntimeError(f"device status {st:#x} after warm-up")
 
@@ -315,11 +348,11 @@ def run_gpu(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(steps):
+        pre(stream)
         ev_s[k].record(stream)
-        mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
-                out, lse, ws, stream)
+        fwd_call(stream)
         ev_f[k].record(stream)
-        mla.combine(plan, t["lens"], out, lse, ws, stream)
+        post(stream)
         ev_e[k].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -330,7 +363,7 @@ def run_gpu(args):
     total_s = t_start.elapsed_time(t_end) / 1e3
     fwd_ms = [ev_s[k].elapsed_time(ev_f[k]) for k in range(steps)]
     step_ms = [ev_s[k].elapsed_time(ev_e[k]) for k in range(steps)]
-    st = mla.check(plan, ws)
+    st = status()
     if st != 0:
         raise RuntimeError(f"device status {st:#x} after the timed steps")
 
@@ -372,9 +405,9 @@ def run_gpu(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cap = torch.cuda.current_stream()
-            mla.fwd(plan, t["q"], t["cache"], t["scale"], t["bt"], t["lens"], p.softmax_scale,
-                    out, lse, ws, cap)
-            mla.combine(plan, t["lens"], out, lse, ws, cap)
+            pre(cap)
+            fwd_call(cap)
+            post(cap)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
@@ -388,14 +421,14 @@ def run_gpu(args):
         graph = {"us_per_call": gsec / steps * 1e6,
                  "value": aggregate_rate(alg["kv_bytes"] * steps, world, gsec) / 1e12,
                  "unit": UNIT, "steps": steps}
-        st = mla.check(plan, ws)
+        st = status()
         if st != 0:
             raise RuntimeError(f"device status {st:#x} after the graph replays")
 
     # end to end through the public API with host buffers: H2D of q, block
     # table and lengths from pinned memory, decode, D2H of out and lse
-    e2e = None if args.no_e2e else e2e_measure(mla, p, t, plan, ws, stream, dev,
-                                                max(10, min(steps, 400)), world)
+    e2e = None if (args.no_e2e or args.dplan) else e2e_measure(mla, p, t, plan, ws, stream, dev,
+                                                                max(10, min(steps, 400)), world)
 
     line = {
         "metric": METRIC, "value": kv_rate / 1e12, "unit": UNIT, "n_gpus": world,
@@ -403,8 +436,10 @@ def run_gpu(args):
         "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if p.kv_dtype == syn.KV_BF16 else "fp8_e4m3->bf16",
         "data": "synthetic (seeded N(0,1), numpy Philox)",
-        "config": dict(config_of(p, args.workload), splits=plan.num_splits,
-                       chunk_len=plan.chunk_len, num_sms=plan.num_sms),
+        "config": dict(config_of(p, args.workload), **(
+            {"planner": "device", "unit_capacity": plan.max_units, "num_sms": plan.num_sms}
+            if args.dplan else
+            {"splits": plan.num_splits, "chunk_len": plan.chunk_len, "num_sms": plan.num_sms})),
         "roofline": roof, "clocks": clk, "e2e": e2e,
         **({"cuda_graph": graph} if graph is not None else {}),
         "gpu_launches": steps * launches_per_step,
@@ -508,6 +543,67 @@ def e2e_measure(mla, p, t, plan, ws, stream, dev, steps, world):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def run_epilogue_bench(args):
+    """The decode epilogue alone (q-concat + latent-row insert, one token per
+    sequence at decode, H query rows + one cache row per token): µs per call
+    and GB/s moved, CUDA events over back-to-back calls, inputs resident."""
+    import torch
+    import paged_mla_decode_latent_gb300 as mla
+    torch.cuda.set_device(0)
+    mla.build()
+    T, H = args.tokens or 1, args.heads or 8
+    fp8 = args.kv == "fp8"
+    ps, pages = 64, max(4, (4 * T) // 64 + 4)
+    g = np.random.default_rng(0)
+    mk = lambda *sh: torch.randn(*sh, dtype=torch.float32, device="cuda").to(torch.bfloat16)  # noqa: E731
+    ql, qp, kc, kp = mk(T, H, 512), mk(T, H, 64), mk(T, 512), mk(T, 64)
+    slots = torch.from_numpy(g.choice(pages * ps, size=T, replace=False).astype(np.int64)).cuda()
+    q = torch.empty((T, H, 576), dtype=torch.bfloat16, device="cuda")
+    cache = (torch.zeros((pages, ps, 576), dtype=torch.uint8, device="cuda") if fp8 else
+             torch.zeros((pages, ps, 576), dtype=torch.bfloat16, device="cuda"))
+    scale = torch.tensor([0.0123], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    call = lambda s: mla.epilogue(ql, qp, kc, kp, slots, q, cache, scale, stream=s)  # noqa: E731
+    for _ in range(max(3, args.warmup)):
+        call(stream)
+    # Host-side launch cost (the ctypes call) exceeds this kernel's time, so
+    # the calls are captured once as a CUDA graph and replayed: the device
+    # time per call is what is measured.
+    per_graph = 100
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = torch.cuda.current_stream()
+        for _ in range(per_graph):
+            call(cap)
+    g.replay()
+    reps = max(1, (args.steps if args.steps > 0 else 2000) // per_graph)
+    steps = reps * per_graph
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    moved = T * H * 1152 * 2 + T * 1152 + T * (576 if fp8 else 1152) + T * 8
+    hbm, _, _, src = load_peaks()
+    gbs = moved / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "MLA decode epilogue µs/call (q-concat + latent cache insert)", "value": us,
+        "unit": "us", "higher_is_better": False, "steps": steps, "n_gpus": 1,
+        "dtype": "bf16" if not fp8 else "bf16->fp8_e4m3",
+        "config": {"workload": f"epilogue_t{T}_h{H}_{'fp8' if fp8 else 'bf16'}", "tokens": T,
+                   "heads": H, "page_size": ps, "timing": "CUDA graph of 100 calls, replayed",
+                   "l2": "working set %.1f MB: L2-resident (decode-size call)" % (moved / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "bytes_per_call": moved, "peak_source": src},
+        "context": {"b300_page_kernel_us": 2.06,
+                    "note": "the page's fused epilogue on B300, Kimi-K3 TP8 decode at concurrency 1"},
+        "gpu_launches": steps}))
+    return 0
+
+
 def kernel_revision() -> str:
     """Hash of the kernel sources: traffic figures are void once it changes."""
     import hashlib
@@ -562,12 +658,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense",
-                    choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp"])
+                    choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp", "epilogue"])
+    ap.add_argument("--tokens", type=int, default=0, help="epilogue workload: tokens (default 1)")
+    ap.add_argument("--heads", type=int, default=0, help="epilogue workload: heads (default 8)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="epilogue workload: cache")
     ap.add_argument("--batch", type=int, default=0, help="dense workload: batch (default 64)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="dense (default 8192) or fp8_long (default 109440) workload: context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--dplan", action="store_true",
+                    help="device-planned path: the partition computed on the GPU each step")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured as one CUDA graph and replayed")
     args = ap.parse_args(argv)
@@ -579,6 +680,8 @@ def main(argv=None):
                          "per GPU with --nproc-per-node equal to --gpus")
     if args.launch_check:
         return run_launch_check(args)
+    if args.workload == "epilogue":
+        return run_epilogue_bench(args)
     if args.impl == "reference":
         if args.steps <= 0:
             args.steps = 3

@@ -206,6 +206,188 @@ int mla_decode_check(const mla_decode_plan_t* plan, const void* workspace, void*
                      int32_t* host_status);
 
 /*
+ * Device-planned decode.  The three calls of "HK MLA: MI35x m16x8 retune, new
+ * m16x4 kernel, page_size + mask support" (aiter PR 3072), Summary, track 2:
+ * a sizes query, a metadata kernel on the device and the launch, agreeing on
+ * the work-slot count tied to the SM count:
+ *
+ *   mla_decode_dplan_info      host: sizes from capacities only (no lengths)
+ *   mla_decode_plan_device     device: the split-KV partition from the device
+ *                              lengths, written into the workspace
+ *   mla_decode_fwd_dplan       the decode over a grid of max_units CTA pairs,
+ *                              each taking its unit from the list (slots past
+ *                              the list's length exit at once)
+ *   mla_decode_combine_dplan   the merge of the sequences that were cut
+ *
+ * Nothing queued depends on the lengths' values, so a CUDA graph of the last
+ * three calls stays valid whatever the lengths become, up to ctx_capacity.
+ * The partition: with P = num_sms / 2 pairs and K = the batch's 64-key tiles,
+ * sequences are cut into chunks of max(ceil(K / P), 2) tiles unless none is
+ * longer than 5/4 of that share (then none is cut); units are listed chunk
+ * level by chunk level, sequences with more chunks first.  At most P + B
+ * chunks, so max_units = row_blocks * (P + B).
+ *
+ * Page tables: the padded block table of mla_decode_fwd (kv_indptr NULL), or
+ * the CSR form: kv_indptr device int32 [B + 1], sequence b's page ids are
+ * block_table[kv_indptr[b] .. kv_indptr[b + 1]) (block_table is kv_indices,
+ * bt_stride ignored) and its context is clamped, and flagged, to those pages.
+ */
+typedef struct mla_decode_dplan_t {
+  int32_t version;        /* MLA_DECODE_DPLAN_VERSION */
+  int32_t batch;          /* B, 1 .. 1024 */
+  int32_t num_heads, sq, page_size, kv_dtype, causal;
+  int32_t rows;           /* H * Sq */
+  int32_t row_blocks;     /* ceil(rows / 128) */
+  int32_t ctx_capacity;   /* longest context any call may bring */
+  int32_t num_sms;        /* SMs the partition is balanced for */
+  int32_t pairs;          /* P = num_sms / 2 (at most 255) */
+  int32_t max_parts;      /* partial-slot capacity, P + B */
+  int32_t max_units;      /* work-list capacity and launch size, row_blocks * (P + B) */
+  int32_t min_chunk_keys; /* shortest chunk a cut sequence gets (128) */
+  int32_t wait_limit_us;  /* as in mla_decode_plan_t: 0 = 2 s; the one field a caller may set */
+  int64_t ws_units_offset;  /* int32x4 [max_units] {b, row block | chunk << 8, k0, k1} */
+  int64_t ws_seq_offset;    /* int32x4 [B] {clamped ctx, first partial slot, chunks, 0} */
+  int64_t ws_count_offset;  /* int32 [4] {units, chunk keys, partial slots used, 0} */
+  int64_t ws_partial_o_offset;   /* fp32 [max_parts, rows, 512] */
+  int64_t ws_partial_lse_offset; /* fp32 [max_parts, rows] */
+  int64_t ws_status_offset;      /* int32 status word */
+  int64_t workspace_bytes;
+} mla_decode_dplan_t;
+
+#define MLA_DECODE_DPLAN_VERSION 1
+
+/* Sizes of the device-planned decode (pure host code; num_sms 0 queries the
+ * current device).  Arguments as mla_decode_plan, with ctx_capacity in place
+ * of the lengths.  Returns MLA_OK, MLA_ERR_INVALID_ARG or MLA_ERR_CUDA. */
+int mla_decode_dplan_info(int32_t batch, int32_t num_heads, int32_t sq, int32_t page_size,
+                          int32_t kv_dtype, int32_t causal, int32_t ctx_capacity,
+                          int32_t num_sms, mla_decode_dplan_t* info);
+
+/* The partition on the device: reads seq_lens (device int32 [B]) and, in the
+ * CSR form, kv_indptr (else NULL); resets the status word and writes the
+ * unit list into the workspace (256-byte aligned, >= workspace_bytes).
+ * Lengths < 0 or beyond the capacity (or the sequence's CSR pages) are
+ * clamped and set MLA_DEVFLAG_CTX_RANGE. */
+int mla_decode_plan_device(const mla_decode_dplan_t* dplan, const int32_t* seq_lens,
+                           const int32_t* kv_indptr, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* The decode over the device-written unit list: arguments as mla_decode_fwd
+ * (the lengths come from the plan in the workspace) plus kv_indptr for the
+ * CSR form.  Units of uncut sequences write out and lse; cut ones write
+ * partials for mla_decode_combine_dplan, which must follow. */
+int mla_decode_fwd_dplan(const mla_decode_dplan_t* dplan, const void* q, const void* kv_cache,
+                         int64_t num_pages, const float* kv_scale, const int32_t* block_table,
+                         int64_t bt_stride, const int32_t* kv_indptr, float softmax_scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* The log-sum-exp merge of the cut sequences (the others return at once). */
+int mla_decode_combine_dplan(const mla_decode_dplan_t* dplan, void* workspace,
+                             size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/*
+ * mla_gather_kv_b_proj -- cached-prefix expansion of the paged latent into
+ * full per-head keys and values through kv_b_proj ("perf(mla): chunk the
+ * non-FP4 gather_kv_b_proj over KV", aiter PR 4776, description): for
+ * sequence b, cached token j < seq_lens[b] and head h,
+ *
+ *   c_j = latent dims 0..511 of the token's cache row, r_j = rope dims 512..575
+ *         (fp8 codes times kv_scale)
+ *   k[t, h, 0:128]   = W[h, 0:128, :] c_j      k[t, h, 128:192] = r_j
+ *   v[t, h, 0:128]   = W[h, 128:256, :] c_j
+ *
+ * with t = cu_seqlens[b] + j (the valid tokens, packed sequence by sequence).
+ * One CTA per (sequence, 128-token chunk, group of 16 heads) on a grid sized
+ * from max_ctx; chunks past a sequence's end return at once.  bf16 MMAs with
+ * fp32 accumulation; k and v are rounded to bf16.
+ *
+ * kv_cache, num_pages, page_size, kv_dtype, kv_scale, block_table, bt_stride
+ *              as mla_decode_fwd
+ * seq_lens     device int32 [B], each <= max_ctx (larger values are clamped
+ *              and set MLA_DEVFLAG_CTX_RANGE)
+ * cu_seqlens   device int32 [B + 1], the exclusive prefix sums of seq_lens
+ * max_ctx      host: the grid's extent, <= bt_stride * page_size
+ * w_kv_b       device bf16 [H, 256, 512]: each head's 128 key rows, then its
+ *              128 value rows (16-byte aligned)
+ * k_out        device bf16 [cu_seqlens[B], H, 192]; v_out bf16 [.., H, 128]
+ * status       device int32 status word (bad page ids, contexts, timeouts);
+ *              the caller clears it
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA.
+ */
+int mla_gather_kv_b_proj(const void* kv_cache, int64_t num_pages, int32_t page_size,
+                         int32_t kv_dtype, const float* kv_scale, const int32_t* block_table,
+                         int64_t bt_stride, const int32_t* seq_lens, const int32_t* cu_seqlens,
+                         int32_t batch, int32_t max_ctx, const void* w_kv_b, int32_t num_heads,
+                         void* k_out, void* v_out, int32_t* status, void* stream);
+
+/*
+ * mla_decode_epilogue -- the step just before the decode on every layer:
+ * writes the 576-wide query rows and inserts each new token's latent row
+ * into the paged cache.  "[Perf][Kimi-K3] Cut MLA decode concat/cache
+ * epilogue latency" (vLLM PR 54896), Purpose items 1-3: the q-concat and
+ * latent cache insert between the absorbed-q GEMM and the decode, bf16 or
+ * fp8 cache, launched as a programmatic dependent of the GEMM.
+ *
+ *   q_out[t, h, 0:512]   = ql_nope[t, h, :]     q_out[t, h, 512:576] = q_pe[t, h, :]
+ *   row                  = kv_c[t, :] || k_pe[t, :]                     (576 wide)
+ *   cache[slot / page_size][slot % page_size][:] = row                  bf16 cache
+ *                                              = e4m3(row / kv_scale)   fp8 cache
+ * with slot = slot_mapping[t]; slot < 0 (a padding token) writes nothing.
+ * The fp8 code is round-to-nearest-even of the fp32 quotient (correctly
+ * rounded fp32 division), saturating to +-448.  q_pe and k_pe are taken as
+ * already rotated (the rope is applied upstream).
+ *
+ * ql_nope      device bf16 [T, H, 512], contiguous, 16-byte aligned
+ * q_pe         device bf16 [T, H, 64]
+ * kv_c         device bf16 [T, 512]
+ * k_pe         device bf16 [T, 64]
+ * slot_mapping device int64 [T]: cache slot of token t (page * page_size + offset)
+ * num_tokens   T >= 0 (0 queues nothing)
+ * num_heads    H, 1 .. 128
+ * q_out        device bf16 [T, H, 576]: the q of mla_decode_fwd
+ * kv_cache     device [num_pages, page_size, 576] bf16 or e4m3 codes
+ * kv_dtype     mla_kv_dtype of the cache; kv_scale device fp32[1] (fp8 only)
+ * cache_inputs_early  1: kv_c and k_pe are older than the kernel this call
+ *              is queued behind, so they are read before the dependency
+ *              wait (as slot_mapping and kv_scale always are); 0: after it
+ * status       optional device int32 status word (NULL = none): a slot
+ *              >= num_pages * page_size is skipped and sets
+ *              MLA_DEVFLAG_BAD_PAGE
+ *
+ * ql_nope and q_pe may be written by the kernel queued just before this one
+ * (the dependency wait covers them); slot_mapping, kv_scale and, with
+ * cache_inputs_early = 1, kv_c and k_pe must be older than that kernel.
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG or MLA_ERR_CUDA.
+ */
+int mla_decode_epilogue(const void* ql_nope, const void* q_pe, const void* kv_c,
+                        const void* k_pe, const int64_t* slot_mapping, int32_t num_tokens,
+                        int32_t num_heads, void* q_out, void* kv_cache, int64_t num_pages,
+                        int32_t page_size, int32_t kv_dtype, const float* kv_scale,
+                        int32_t cache_inputs_early, int32_t* status, void* stream);
+
+/*
+ * mla_decode_step -- one decode of the layer: mla_decode_epilogue for the
+ * plan's batch * Sq new tokens (writing q and the new cache rows), then
+ * mla_decode_fwd and mla_decode_combine, each kernel launched as a
+ * programmatic dependent of the one before (the status word is reset before
+ * the epilogue, so nothing but kernels sits between them on the stream).
+ * The pages' chain of absorbed-q GEMM -> q-concat + cache insert -> decode,
+ * "[Perf][Kimi-K3] Cut MLA decode concat/cache epilogue latency", Purpose.
+ *
+ * Arguments: the epilogue's inputs (T = plan->batch * plan->sq tokens in
+ * sequence-major order, H = plan->num_heads), then those of mla_decode_fwd.
+ * q is written here and read by the decode.  seq_lens count the new tokens,
+ * whose rows this call inserts.  Returns as mla_decode_fwd.
+ */
+int mla_decode_step(const mla_decode_plan_t* plan, const void* ql_nope, const void* q_pe,
+                    const void* kv_c, const void* k_pe, const int64_t* slot_mapping,
+                    int32_t cache_inputs_early, void* q, void* kv_cache, int64_t num_pages,
+                    const float* kv_scale, const int32_t* block_table, int64_t bt_stride,
+                    const int32_t* seq_lens, float softmax_scale, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_fwd_noalloc -- mla_decode_fwd followed by mla_decode_combine,
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart of this call.

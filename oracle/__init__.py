@@ -68,6 +68,14 @@ def _bind(path: str):
     lib.mla_oracle_decode_row.restype = None
     lib.mla_oracle_lse_merge.argtypes = [c_p, c_p, i32, i64, c_p, c_p]
     lib.mla_oracle_lse_merge.restype = None
+    lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.mla_oracle_epilogue.argtypes = [c_p, c_p, c_p, c_p, c_p, i32, i32, c_p, c_p, i64, i32,
+                                        i32, ctypes.c_float]
+    lib.mla_oracle_epilogue.restype = None
+    lib.mla_oracle_gather_kv_b_proj.argtypes = [c_p, i32, f64, i32, c_p, i64, c_p, c_p, i32, c_p,
+                                                i32, c_p, c_p]
+    lib.mla_oracle_gather_kv_b_proj.restype = None
     return lib
 
 
@@ -94,7 +102,8 @@ def compile_variant(src_text: str, workdir: str):
                    check=True, capture_output=True, text=True)
     bound = _bind(lib)
     ns = types.SimpleNamespace(KV_BF16=KV_BF16, KV_FP8_E4M3=KV_FP8_E4M3)
-    for name in ("bf16_to_double", "e4m3_to_double", "decode", "decode_row", "lse_merge"):
+    for name in ("bf16_to_double", "e4m3_to_double", "decode", "decode_row", "lse_merge",
+                 "e4m3_encode", "epilogue", "gather_kv_b_proj"):
         fn = globals()[name]
         ns.__dict__[name] = (lambda f: (lambda *a, **k: f(*a, _lib=bound, **k)))(fn)
     return ns
@@ -185,3 +194,56 @@ def lse_merge(o_parts, lse_parts, _lib=None):
     lib.mla_oracle_lse_merge(o_parts.ctypes.data, lse_parts.ctypes.data, int(S), int(rows),
                              out.ctypes.data, lse.ctypes.data)
     return out, lse
+
+
+def e4m3_encode(y: float, _lib=None) -> int:
+    """Nearest fp8 E4M3FN code of the binary32 value y (ties to even, saturating)."""
+    return int((_lib or _load()).mla_oracle_e4m3_encode(float(np.float32(y))))
+
+
+def epilogue(ql_nope, q_pe, kv_c, k_pe, slot_mapping, cache, kv_dtype, kv_scale=1.0,
+             _lib=None):
+    """The decode epilogue: returns (q [T, H, 576] bf16 bits, the cache after the
+    inserts).  ql_nope uint16 [T, H, 512], q_pe uint16 [T, H, 64], kv_c uint16
+    [T, 512], k_pe uint16 [T, 64] (bf16 bits), slot_mapping int64 [T], cache
+    uint16 / uint8 [P, ps, 576] (copied, not modified)."""
+    lib = _lib or _load()
+    ql = _c(ql_nope, np.uint16)
+    qp = _c(q_pe, np.uint16)
+    kc = _c(kv_c, np.uint16)
+    kp = _c(k_pe, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    T, H, _ = ql.shape
+    q = np.zeros((T, H, 576), np.uint16)
+    out_cache = np.array(cache, dtype=np.uint16 if kv_dtype == KV_BF16 else np.uint8, copy=True,
+                         order="C")
+    lib.mla_oracle_epilogue(ql.ctypes.data, qp.ctypes.data, kc.ctypes.data, kp.ctypes.data,
+                            sm.ctypes.data, int(T), int(H), q.ctypes.data, out_cache.ctypes.data,
+                            int(out_cache.shape[0]), int(out_cache.shape[1]), int(kv_dtype),
+                            float(np.float32(kv_scale)))
+    return q, out_cache
+
+
+def gather_kv_b_proj(cache, kv_dtype, kv_scale, page_size, block_table, seq_lens, w_bits,
+                     _lib=None):
+    """Per-head keys and values of every cached token: (k [T, H, 192], v [T, H, 128])
+    in float64, T = sum(seq_lens), rows packed sequence by sequence.  w_bits is
+    kv_b_proj as bf16 bits [H, 256, 512] (each head's 128 key rows, then 128
+    value rows)."""
+    lib = _lib or _load()
+    cache = _c(cache, np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    w = _c(w_bits, np.uint16)
+    H = int(w.shape[0])
+    assert w.shape[1:] == (256, 512)
+    cu = np.zeros(len(sl) + 1, np.int32)
+    cu[1:] = np.cumsum(sl)
+    T = int(cu[-1])
+    k = np.zeros((max(T, 1), H, 192), np.float64)
+    v = np.zeros((max(T, 1), H, 128), np.float64)
+    lib.mla_oracle_gather_kv_b_proj(cache.ctypes.data, int(kv_dtype), float(kv_scale),
+                                    int(page_size), bt.ctypes.data, int(bt.shape[1]),
+                                    sl.ctypes.data, cu.ctypes.data, int(len(sl)), w.ctypes.data,
+                                    H, k.ctypes.data, v.ctypes.data)
+    return k[:T], v[:T]

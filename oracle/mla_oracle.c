@@ -35,12 +35,27 @@
  *   - softmax, log-sum-exp and the weighted sum are the textbook definition
  *     of scaled dot-product attention; the pages give no formula of their
  *     own.
+ *   - the cached-prefix expansion (mla_oracle_gather_kv_b_proj): every
+ *     cached latent row of a sequence, gathered through the block table and
+ *     dequantised, multiplied by each head's kv_b_proj block into that head's
+ *     128 no-rope key dims and 128 value dims; the key row is completed by
+ *     the row's 64 rope dims: "perf(mla): chunk the non-FP4 gather_kv_b_proj
+ *     over KV" (aiter PR 4776), description, first and second paragraphs;
+ *   - the decode epilogue (mla_oracle_epilogue): the q-concat of ql_nope and
+ *     q_pe into the 576-wide query row and the insert of the new latent row
+ *     into the paged cache through slot_mapping, bf16 or fp8: "[Perf]
+ *     [Kimi-K3] Cut MLA decode concat/cache epilogue latency" (vLLM PR
+ *     54896), Purpose, items 1-3.
  *
  * Numeric formats decoded here, from their published definitions:
  *   - bfloat16: the upper 16 bits of an IEEE binary32;
  *   - fp8 E4M3FN (OCP 8-bit floating point specification): 1 sign bit,
  *     4 exponent bits with bias 7, 3 mantissa bits, subnormals at exponent
  *     field 0, no infinities, S.1111.111 is NaN, largest finite 448.
+ *     Encoding (mla_oracle_e4m3_encode): the nearest representable value,
+ *     ties to the even code, magnitudes beyond 448 saturated to 448 (the
+ *     "saturating" conversion of the same specification), found by trying
+ *     every code.
  */
 #include <math.h>
 #include <stdint.h>
@@ -241,6 +256,114 @@ void mla_oracle_lse_merge(const double* o_parts, const double* lse_parts, int S,
       w = exp(ls - L);
       for (d = 0; d < ORACLE_D_V; ++d)
         out[r * ORACLE_D_V + d] += w * o_parts[((int64_t)s * rows + r) * ORACLE_D_V + d];
+    }
+  }
+}
+
+/*
+ * binary32 value -> fp8 E4M3FN code, round to nearest, ties to even,
+ * saturating: every non-negative finite code is tried and the nearest kept
+ * (on a tie the code whose last mantissa bit is 0); |y| > 448 gives 448;
+ * NaN gives 0x7F.  The sign bit is the sign of y, so -0 and negative values
+ * that round to zero give 0x80.
+ */
+uint8_t mla_oracle_e4m3_encode(float y) {
+  double a = fabs((double)y);
+  int best = 0, c;
+  double best_err = INFINITY;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  if (isnan(y)) return 0x7F;
+  if (a > 448.0) return (uint8_t)(sign | 0x7E);
+  for (c = 0; c <= 0x7E; ++c) {
+    double err = fabs(a - mla_oracle_e4m3_to_double((uint8_t)c));
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best_err = err;
+      best = c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/*
+ * The decode epilogue for T tokens of H heads:
+ *   q_out[t][h][0:512] = ql_nope[t][h][:],  q_out[t][h][512:576] = q_pe[t][h][:]
+ *   slot = slot_mapping[t]; if 0 <= slot < num_pages * page_size:
+ *     cache[slot / page_size][slot % page_size][d] = x_d            (bf16)
+ *                                                  = e4m3(x_d / s)  (fp8)
+ *   with x = kv_c[t][:] || k_pe[t][:] and x_d / s the binary32 quotient
+ *   (computed in double and rounded once to binary32: the correctly rounded
+ *   single-precision division).  Slots < 0 are padding tokens: no write.
+ */
+void mla_oracle_epilogue(const uint16_t* ql_nope, const uint16_t* q_pe,
+                         const uint16_t* kv_c, const uint16_t* k_pe,
+                         const int64_t* slot_mapping, int T, int H, uint16_t* q_out,
+                         void* cache, int64_t num_pages, int page_size, int kv_dtype,
+                         float kv_scale) {
+  int t, h, d;
+  for (t = 0; t < T; ++t) {
+    for (h = 0; h < H; ++h) {
+      uint16_t* dst = q_out + ((int64_t)t * H + h) * ORACLE_D_QK;
+      for (d = 0; d < 512; ++d) dst[d] = ql_nope[((int64_t)t * H + h) * 512 + d];
+      for (d = 0; d < 64; ++d) dst[512 + d] = q_pe[((int64_t)t * H + h) * 64 + d];
+    }
+    {
+      int64_t slot = slot_mapping[t];
+      int64_t page, off;
+      if (slot < 0 || slot >= num_pages * (int64_t)page_size) continue;
+      page = slot / page_size;
+      off = slot % page_size;
+      for (d = 0; d < ORACLE_D_QK; ++d) {
+        uint16_t x = d < 512 ? kv_c[(int64_t)t * 512 + d] : k_pe[(int64_t)t * 64 + (d - 512)];
+        int64_t idx = (page * page_size + off) * ORACLE_D_QK + d;
+        if (kv_dtype == ORACLE_KV_BF16) {
+          ((uint16_t*)cache)[idx] = x;
+        } else {
+          float y = (float)(mla_oracle_bf16_to_double(x) / (double)kv_scale);
+          ((uint8_t*)cache)[idx] = mla_oracle_e4m3_encode(y);
+        }
+      }
+    }
+  }
+}
+
+/*
+ * Cached-prefix expansion of the paged latent into per-head keys and values:
+ * for sequence b, cached token j < seq_lens[b], head h < H,
+ *   c_j             = dequant(cache[bt[b][j / ps]][j % ps][0:512])
+ *   r_j             = dequant(cache[bt[b][j / ps]][j % ps][512:576])
+ *   k[t, h, 0:128]  = sum_d W[h][0:128][d]   * c_j[d]
+ *   k[t, h, 128:192]= r_j
+ *   v[t, h, 0:128]  = sum_d W[h][128:256][d] * c_j[d]
+ * with output row t = cu_seqlens[b] + j (the valid tokens, packed).
+ * W is [H][256][512] bf16 bits (kv_b_proj, each head's 128 key rows then
+ * 128 value rows); k is [T][H][192], v [T][H][128], in double.
+ */
+void mla_oracle_gather_kv_b_proj(const void* cache, int kv_dtype, double kv_scale,
+                                 int page_size, const int32_t* bt, int64_t bt_stride,
+                                 const int32_t* seq_lens, const int32_t* cu_seqlens, int B,
+                                 const uint16_t* W, int H, double* k, double* v) {
+  int b;
+  for (b = 0; b < B; ++b) {
+    int64_t j, n = seq_lens[b];
+#pragma omp parallel for schedule(dynamic, 16)
+    for (j = 0; j < n; ++j) {
+      double c[ORACLE_D_QK];
+      int64_t t = (int64_t)cu_seqlens[b] + j;
+      int h, o, d;
+      for (d = 0; d < ORACLE_D_QK; ++d)
+        c[d] = cache_elem(cache, kv_dtype, kv_scale, bt, bt_stride, b, page_size, j, d);
+      for (h = 0; h < H; ++h) {
+        for (o = 0; o < 256; ++o) {
+          double acc = 0.0;
+          const uint16_t* w = W + ((int64_t)h * 256 + o) * 512;
+          for (d = 0; d < 512; ++d) acc += mla_oracle_bf16_to_double(w[d]) * c[d];
+          if (o < 128)
+            k[(t * H + h) * 192 + o] = acc;
+          else
+            v[(t * H + h) * 128 + (o - 128)] = acc;
+        }
+        for (d = 0; d < 64; ++d) k[(t * H + h) * 192 + 128 + d] = c[512 + d];
+      }
     }
   }
 }

@@ -8,7 +8,10 @@ the library is missing, every call raises.
 
 Names follow the C ABI: ``plan`` -> ``mla_decode_plan``, ``fwd`` ->
 ``mla_decode_fwd``, ``combine`` -> ``mla_decode_combine``, ``check`` ->
-``mla_decode_check``.  ``decode`` is plan + fwd + combine with freshly
+``mla_decode_check``, ``epilogue`` -> ``mla_decode_epilogue``, ``step`` ->
+``mla_decode_step``; the device-planned path: ``dplan_info``, ``plan_device``,
+``fwd_dplan`` and ``combine_dplan``; ``gather_kv_b_proj`` ->
+``mla_gather_kv_b_proj``.  ``decode`` is plan + fwd + combine with freshly
 allocated outputs and workspace, for convenience.
 """
 from __future__ import annotations
@@ -40,8 +43,10 @@ DEVFLAG_Q_RANGE = 0x8
 
 # Every symbol include/mla_decode.h declares.
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_fwd", "mla_decode_combine",
-                    "mla_decode_check", "mla_decode_fwd_noalloc", "mla_status_string",
-                    "mla_decode_version")
+                    "mla_decode_check", "mla_decode_dplan_info", "mla_decode_plan_device",
+                    "mla_decode_fwd_dplan", "mla_decode_combine_dplan", "mla_decode_epilogue",
+                    "mla_decode_step", "mla_gather_kv_b_proj", "mla_decode_fwd_noalloc",
+                    "mla_status_string", "mla_decode_version")
 
 
 class Plan(ctypes.Structure):
@@ -52,6 +57,20 @@ class Plan(ctypes.Structure):
         "cluster_size", "grid_x", "grid_y", "grid_z", "wait_limit_us")] + [
         (n, ctypes.c_int64) for n in (
             "ws_partial_o_offset", "ws_partial_lse_offset", "ws_status_offset", "workspace_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class DPlan(ctypes.Structure):
+    """Mirror of ``mla_decode_dplan_t`` (plain old data)."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "version", "batch", "num_heads", "sq", "page_size", "kv_dtype", "causal", "rows",
+        "row_blocks", "ctx_capacity", "num_sms", "pairs", "max_parts", "max_units",
+        "min_chunk_keys", "wait_limit_us")] + [
+        (n, ctypes.c_int64) for n in (
+            "ws_units_offset", "ws_seq_offset", "ws_count_offset", "ws_partial_o_offset",
+            "ws_partial_lse_offset", "ws_status_offset", "workspace_bytes")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -91,6 +110,25 @@ def lib():
     L.mla_decode_combine.restype = ctypes.c_int
     L.mla_decode_fwd_noalloc.argtypes = [P, vp, vp, i64, vp, vp, i64, vp, f32, vp, vp, vp]
     L.mla_decode_fwd_noalloc.restype = ctypes.c_int
+    D = ctypes.POINTER(DPlan)
+    L.mla_decode_dplan_info.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, D]
+    L.mla_decode_dplan_info.restype = ctypes.c_int
+    L.mla_decode_plan_device.argtypes = [D, vp, vp, vp, ctypes.c_size_t, vp]
+    L.mla_decode_plan_device.restype = ctypes.c_int
+    L.mla_decode_fwd_dplan.argtypes = [D, vp, vp, i64, vp, vp, i64, vp, f32, vp, vp, vp,
+                                       ctypes.c_size_t, vp]
+    L.mla_decode_fwd_dplan.restype = ctypes.c_int
+    L.mla_decode_combine_dplan.argtypes = [D, vp, ctypes.c_size_t, vp, vp, vp]
+    L.mla_decode_combine_dplan.restype = ctypes.c_int
+    L.mla_gather_kv_b_proj.argtypes = [vp, i64, i32, i32, vp, vp, i64, vp, vp, i32, i32, vp, i32,
+                                       vp, vp, vp, vp]
+    L.mla_gather_kv_b_proj.restype = ctypes.c_int
+    L.mla_decode_epilogue.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, i32, i32, vp,
+                                      i32, vp, vp]
+    L.mla_decode_epilogue.restype = ctypes.c_int
+    L.mla_decode_step.argtypes = [P, vp, vp, vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, vp, f32,
+                                  vp, vp, vp, ctypes.c_size_t, vp]
+    L.mla_decode_step.restype = ctypes.c_int
     L.mla_decode_check.argtypes = [P, vp, vp, ctypes.POINTER(i32)]
     L.mla_decode_check.restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
@@ -155,6 +193,97 @@ def combine(p: Plan, seq_lens, out, lse, workspace, stream=None) -> None:
         ctypes.byref(p), _ptr(seq_lens), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _ptr(out), _ptr(lse), _stream(stream))
     _raise(st, "mla_decode_combine")
+
+
+def dplan_info(batch: int, num_heads: int, sq: int, page_size: int, kv_dtype: int = KV_BF16,
+               causal: bool = False, ctx_capacity: int = 0, num_sms: int = 0) -> DPlan:
+    """``mla_decode_dplan_info``: sizes of the device-planned decode."""
+    d = DPlan()
+    st = lib().mla_decode_dplan_info(int(batch), int(num_heads), int(sq), int(page_size),
+                                     int(kv_dtype), int(bool(causal)), int(ctx_capacity),
+                                     int(num_sms), ctypes.byref(d))
+    _raise(st, "mla_decode_dplan_info")
+    return d
+
+
+def _ws_bytes(workspace):
+    return int(workspace.numel() * workspace.element_size())
+
+
+def plan_device(d: DPlan, seq_lens, workspace, kv_indptr=None, stream=None) -> None:
+    """``mla_decode_plan_device``: the partition, computed on the GPU."""
+    st = lib().mla_decode_plan_device(ctypes.byref(d), _ptr(seq_lens), _ptr(kv_indptr),
+                                      _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+    _raise(st, "mla_decode_plan_device")
+
+
+def fwd_dplan(d: DPlan, q, kv_cache, kv_scale, block_table, softmax_scale: float, out, lse,
+              workspace, kv_indptr=None, stream=None) -> None:
+    """``mla_decode_fwd_dplan``; block_table is kv_indices when kv_indptr is given."""
+    stride = int(block_table.stride(0)) if block_table.dim() == 2 else 1
+    st = lib().mla_decode_fwd_dplan(
+        ctypes.byref(d), _ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_scale),
+        _ptr(block_table), stride, _ptr(kv_indptr), float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), _ws_bytes(workspace), _stream(stream))
+    _raise(st, "mla_decode_fwd_dplan")
+
+
+def combine_dplan(d: DPlan, out, lse, workspace, stream=None) -> None:
+    """``mla_decode_combine_dplan``."""
+    st = lib().mla_decode_combine_dplan(ctypes.byref(d), _ptr(workspace), _ws_bytes(workspace),
+                                        _ptr(out), _ptr(lse), _stream(stream))
+    _raise(st, "mla_decode_combine_dplan")
+
+
+def dplan_check(d: DPlan, workspace, stream=None) -> int:
+    """Device status bits of the last device-planned call (blocks until the stream drains)."""
+    import torch
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    off = int(d.ws_status_offset)
+    return int(workspace[off:off + 4].view(torch.int32).item())
+
+
+def gather_kv_b_proj(kv_cache, kv_scale, block_table, seq_lens, cu_seqlens, max_ctx: int, w_kv_b,
+                     k_out, v_out, status, stream=None) -> None:
+    """``mla_gather_kv_b_proj``: k_out [T, H, 192], v_out [T, H, 128] bf16 from the
+    paged latent and kv_b_proj w_kv_b [H, 256, 512] bf16."""
+    import torch
+    fp8 = kv_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    st = lib().mla_gather_kv_b_proj(
+        _ptr(kv_cache), int(kv_cache.shape[0]), int(kv_cache.shape[1]),
+        KV_FP8_E4M3 if fp8 else KV_BF16, _ptr(kv_scale), _ptr(block_table),
+        int(block_table.stride(0)), _ptr(seq_lens), _ptr(cu_seqlens), int(seq_lens.numel()),
+        int(max_ctx), _ptr(w_kv_b), int(w_kv_b.shape[0]), _ptr(k_out), _ptr(v_out), _ptr(status),
+        _stream(stream))
+    _raise(st, "mla_gather_kv_b_proj")
+
+
+def epilogue(ql_nope, q_pe, kv_c, k_pe, slot_mapping, q_out, kv_cache, kv_scale=None,
+             cache_inputs_early: bool = False, status=None, stream=None) -> None:
+    """``mla_decode_epilogue``: q_out = ql_nope || q_pe; cache[slot] = kv_c || k_pe
+    (bf16, or e4m3 codes of x / kv_scale for a uint8 / float8 cache)."""
+    import torch
+    T, H, _ = ql_nope.shape
+    fp8 = kv_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    st = lib().mla_decode_epilogue(
+        _ptr(ql_nope), _ptr(q_pe), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), int(T), int(H),
+        _ptr(q_out), _ptr(kv_cache), int(kv_cache.shape[0]), int(kv_cache.shape[1]),
+        KV_FP8_E4M3 if fp8 else KV_BF16, _ptr(kv_scale), int(bool(cache_inputs_early)),
+        _ptr(status), _stream(stream))
+    _raise(st, "mla_decode_epilogue")
+
+
+def step(p: Plan, ql_nope, q_pe, kv_c, k_pe, slot_mapping, q, kv_cache, kv_scale, block_table,
+         seq_lens, softmax_scale: float, out, lse, workspace, cache_inputs_early: bool = False,
+         stream=None) -> None:
+    """``mla_decode_step``: epilogue, fwd and combine chained by programmatic launches."""
+    st = lib().mla_decode_step(
+        ctypes.byref(p), _ptr(ql_nope), _ptr(q_pe), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping),
+        int(bool(cache_inputs_early)), _ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]),
+        _ptr(kv_scale), _ptr(block_table), int(block_table.stride(0)), _ptr(seq_lens),
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _raise(st, "mla_decode_step")
 
 
 def check(p: Plan, workspace, stream=None) -> int:

@@ -36,13 +36,15 @@ int check_workspace(const mla_decode_plan_t* plan, const void* ws, size_t bytes)
   return MLA_OK;
 }
 
-}  // namespace
-
-extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
-                              int64_t num_pages, const float* kv_scale,
-                              const int32_t* block_table, int64_t bt_stride,
-                              const int32_t* seq_lens, float softmax_scale, void* out, float* lse,
-                              void* workspace, size_t workspace_bytes, void* stream) {
+// Validation and launch of the decode kernel.  reset_status: queue the
+// status word's reset first (mla_decode_step resets it before the epilogue
+// instead, so that no memset node sits between the epilogue and this kernel
+// and the programmatic dependent launch can take effect).
+int fwd_impl(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
+             int64_t num_pages, const float* kv_scale, const int32_t* block_table,
+             int64_t bt_stride, const int32_t* seq_lens, float softmax_scale, void* out,
+             float* lse, void* workspace, size_t workspace_bytes, void* stream,
+             bool reset_status) {
   int st = check_plan(plan);
   if (st != MLA_OK) return st;
   st = check_workspace(plan, workspace, workspace_bytes);
@@ -74,6 +76,11 @@ extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, cons
   p.status = reinterpret_cast<int32_t*>(ws + plan->ws_status_offset);
   p.wait_ns = plan->wait_limit_us > 0 ? (uint64_t)plan->wait_limit_us * 1000ull
                                       : kDefaultWaitNs;
+  p.units = nullptr;
+  p.n_units = nullptr;
+  p.seq_info = nullptr;
+  p.bt_indptr = nullptr;
+  p.unit_capacity = 0;
   p.batch = plan->batch;
   p.heads = plan->num_heads;
   p.sq = plan->sq;
@@ -87,9 +94,47 @@ extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, cons
   p.row_blocks = plan->row_blocks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (reset_status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (mla_launch_fwd(p, stream) != 0) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_fwd(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
+                              int64_t num_pages, const float* kv_scale,
+                              const int32_t* block_table, int64_t bt_stride,
+                              const int32_t* seq_lens, float softmax_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(plan, q, kv_cache, num_pages, kv_scale, block_table, bt_stride, seq_lens,
+                  softmax_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+extern "C" int mla_decode_step(const mla_decode_plan_t* plan, const void* ql_nope,
+                               const void* q_pe, const void* kv_c, const void* k_pe,
+                               const int64_t* slot_mapping, int32_t cache_inputs_early, void* q,
+                               void* kv_cache, int64_t num_pages, const float* kv_scale,
+                               const int32_t* block_table, int64_t bt_stride,
+                               const int32_t* seq_lens, float softmax_scale, void* out, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != MLA_OK) return st;
+  if (plan->kv_dtype == MLA_KV_FP8_E4M3 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  int32_t* status =
+      reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan->ws_status_offset);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
+  st = mla_decode_epilogue(ql_nope, q_pe, kv_c, k_pe, slot_mapping, plan->batch * plan->sq,
+                           plan->num_heads, q, kv_cache, num_pages, plan->page_size,
+                           plan->kv_dtype, kv_scale, cache_inputs_early, status, stream);
+  if (st != MLA_OK) return st;
+  st = fwd_impl(plan, q, kv_cache, num_pages, kv_scale, block_table, bt_stride, seq_lens,
+                softmax_scale, out, lse, workspace, workspace_bytes, stream, false);
+  if (st != MLA_OK) return st;
+  return mla_decode_combine(plan, seq_lens, workspace, workspace_bytes, out, lse, stream);
 }
 
 extern "C" int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens,
@@ -107,6 +152,7 @@ extern "C" int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* 
   c.part_lse = reinterpret_cast<const float*>(ws + plan->ws_partial_lse_offset);
   c.out = static_cast<uint16_t*>(out);
   c.lse = lse;
+  c.seq_info = nullptr;
   c.batch = plan->batch;
   c.rows = plan->rows;
   c.num_splits = plan->num_splits;

@@ -22,7 +22,6 @@ namespace {
 __global__ void __launch_bounds__(128) combine_kernel(mla::CombineParams p) {
   const int r = blockIdx.x;
   const int b = blockIdx.y;
-  const int S = p.num_splits;
   __shared__ float w_s[mla::kMaxSplits];
   __shared__ float red[4];
   __shared__ float L_s;
@@ -31,7 +30,18 @@ __global__ void __launch_bounds__(128) combine_kernel(mla::CombineParams p) {
   // unless this grid was launched as a programmatic dependent launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const float* lse_row = p.part_lse + (size_t)b * S * p.rows + r;
+  // Splits of this sequence and the first one's partial slot: every
+  // sequence has num_splits slots (host plan), or the device plan's count
+  // (a sequence in one piece was written to out by the decode itself).
+  int S = p.num_splits;
+  size_t part0 = (size_t)b * S;
+  if (p.seq_info != nullptr) {
+    const int4 si = p.seq_info[b];
+    if (si.z <= 1) return;
+    S = si.z;
+    part0 = (size_t)si.y;
+  }
+  const float* lse_row = p.part_lse + part0 * p.rows + r;
   float m = -INFINITY;
   for (int s = threadIdx.x; s < S; s += blockDim.x) m = fmaxf(m, lse_row[(size_t)s * p.rows]);
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -60,8 +70,7 @@ __global__ void __launch_bounds__(128) combine_kernel(mla::CombineParams p) {
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* o_base =
-      reinterpret_cast<const float4*>(p.part_o + ((size_t)b * S * p.rows + r) * mla::kDV) +
-      threadIdx.x;
+      reinterpret_cast<const float4*>(p.part_o + (part0 * p.rows + r) * mla::kDV) + threadIdx.x;
   const size_t stride = (size_t)p.rows * (mla::kDV / 4);
   // Eight splits' partial rows in flight at a time.  An empty split's row
   // holds anything (it was never written): its load is skipped and its

@@ -275,19 +275,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int rb = blockIdx.x >> 1, b = blockIdx.y, split = blockIdx.z;
-
-  // A context the plan does not cover is clamped to [0, max_ctx] and
-  // flagged.  max_ctx keys fit the block table (bt_stride * page_size >=
-  // max_ctx is checked on the host) and the splits (num_splits * chunk_len
-  // >= max_ctx), so no table entry past the sequence's row is read.
-  int ctx = p.seq_lens[b];
-  if (ctx < 0 || ctx > p.max_ctx) {
-    if (threadIdx.x == 0 && rank == 0 && split == 0) atomicOr(p.status, MLA_DEVFLAG_CTX_RANGE);
-    ctx = ctx < 0 ? 0 : p.max_ctx;
+  // The work unit: (sequence b, row block rb, key range [k0, k1)), its
+  // context, and where its result goes (the final output when the unit
+  // covers the whole sequence, else partial slot `part` for the merge).
+  int rb, b, ctx, k0, k1;
+  bool single;
+  size_t part;
+  if (p.units != nullptr) {
+    // Device-planned: the unit list was written by the planning kernel this
+    // one is launched behind, so wait for it first.  Both CTAs of a pair
+    // read the same unit and take the same branches.
+    ptx::grid_dependency_wait();
+    const int u = blockIdx.x >> 1;
+    if (u >= *p.n_units) return;
+    const int4 d = p.units[u];
+    const int4 si = p.seq_info[d.x];
+    b = d.x;
+    rb = d.y & 0xFF;
+    k0 = d.z;
+    k1 = d.w;
+    ctx = si.x;  // already clamped to what the table holds
+    single = si.z == 1;
+    part = (size_t)si.y + (d.y >> 8);
+  } else {
+    rb = blockIdx.x >> 1;
+    b = blockIdx.y;
+    const int split = blockIdx.z;
+    // A context the plan does not cover is clamped to [0, max_ctx] and
+    // flagged.  max_ctx keys fit the block table (bt_stride * page_size >=
+    // max_ctx is checked on the host) and the splits (num_splits *
+    // chunk_len >= max_ctx), so no table entry past the sequence's row is
+    // read.
+    ctx = p.seq_lens[b];
+    if (ctx < 0 || ctx > p.max_ctx) {
+      if (threadIdx.x == 0 && rank == 0 && split == 0) atomicOr(p.status, MLA_DEVFLAG_CTX_RANGE);
+      ctx = ctx < 0 ? 0 : p.max_ctx;
+    }
+    k0 = split * p.chunk_len;
+    k1 = min(k0 + p.chunk_len, ctx);
+    single = p.num_splits == 1;
+    part = (size_t)b * p.num_splits + split;
   }
-  const int k0 = split * p.chunk_len;
-  const int k1 = min(k0 + p.chunk_len, ctx);
   const int n_tiles = k1 > k0 ? (k1 - k0 + T - 1) / T : 0;
   const int vdim0 = (int)rank * 256;  // this CTA's value dims
   const float s_kv = (p.kv_dtype == MLA_KV_FP8_E4M3 && p.kv_scale) ? *p.kv_scale : 1.f;
@@ -295,15 +323,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (n_tiles == 0) {
     // No key of this split: the row results are out = 0, lse = -inf.  Both
     // CTAs of the pair take this branch together, before any cluster traffic.
+    ptx::grid_dependency_wait();
     for (int i = threadIdx.x; i < mla::kRowTile; i += kThreads) {
       const int row = rb * mla::kRowTile + i;
       if (row >= p.rows) break;
-      if (p.num_splits == 1) {
+      if (single) {
         uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
         for (int c = 0; c < 32; ++c) o[c] = make_uint4(0, 0, 0, 0);
         if (rank == 0) p.lse[(size_t)b * p.rows + row] = -INFINITY;
       } else if (rank == 0) {
-        p.part_lse[((size_t)b * p.num_splits + split) * p.rows + row] = -INFINITY;
+        p.part_lse[part * p.rows + row] = -INFINITY;
       }
     }
     return;
@@ -336,6 +365,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   ptx::cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
   ptx::tc_fence_after();
+  // q and the newest cache rows may come from the kernel this one is
+  // launched behind (the decode epilogue): nothing past this point reads
+  // them, or writes an output, before that kernel has completed.  A no-op
+  // when the launch is not a programmatic dependent one.
+  ptx::grid_dependency_wait();
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort, p.wait_ns};
 
@@ -443,7 +477,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // In the rope slab a CTA copies only its 32 dims: the lanes of 16-byte
     // pieces 4 rank .. 4 rank + 3 (bf16) or of 16-code pieces 2 rank, 2 rank + 1 (fp8).
     const bool rope_lane = (kFp8 ? (sub >> 1) : (sub >> 2)) == (int)rank;
-    const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
+    // This sequence's page ids: a row of the padded table, or (CSR form)
+    // kv_indices from kv_indptr[b] on.
+    const int32_t* bt = p.bt + (p.bt_indptr ? (size_t)p.bt_indptr[b] : (size_t)b * p.bt_stride);
     const char* cache = static_cast<const char*>(p.cache);
     auto key_of = [&](int tile, int i) -> int {  // i-th key of this lane, clamped to the split
       const int start = k0 + tile * T;
@@ -848,9 +884,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float invA = lA > 0.f ? s_kv / lA : 0.f, invB = lB > 0.f ? s_kv / lB : 0.f;
       const int rowA = rb * mla::kRowTile + rA, rowB = rb * mla::kRowTile + rB;
       const bool okA = rowA < p.rows, okB = rowB < p.rows;
-      const bool single = p.num_splits == 1;
-      const size_t pA = ((size_t)b * p.num_splits + split) * p.rows + rowA;
-      const size_t pB = ((size_t)b * p.num_splits + split) * p.rows + rowB;
+      const size_t pA = part * p.rows + rowA;
+      const size_t pB = part * p.rows + rowB;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t o[32];
@@ -914,8 +949,19 @@ int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream) {
   e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, fp8 ? 1 : 0);
   if (e != cudaSuccess) return (int)e;
   // Splits vary slowest, so every sequence's first chunk is dispatched
-  // before any second chunk (the planner simulates this order).
-  dim3 grid(p.row_blocks * 2, p.batch, p.num_splits);
-  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
-  return (int)cudaGetLastError();
+  // before any second chunk (the planner simulates this order).  Launched as
+  // a programmatic dependent: behind the decode epilogue the prologue
+  // (barrier set-up, TMEM allocation) overlaps that kernel's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = p.units != nullptr ? dim3(2 * p.unit_capacity, 1, 1)
+                                  : dim3(p.row_blocks * 2, p.batch, p.num_splits);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, kernel, p);
 }

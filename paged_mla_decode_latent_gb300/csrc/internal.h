@@ -33,6 +33,14 @@ struct FwdParams {
   float* part_lse;          // fp32 [B, S, rows]      (S > 1)
   int32_t* status;          // device status word
   uint64_t wait_ns;         // bound of every pipeline wait inside the kernel
+  // Device-planned launches (nullptr otherwise): the unit list
+  // {b, rb | chunk << 8, k0, k1}, its length, and per sequence
+  // {clamped ctx, first partial slot, chunks, 0}.
+  const int4* units;
+  const int32_t* n_units;
+  const int4* seq_info;
+  const int32_t* bt_indptr;  // CSR row starts into bt (kv_indices), or nullptr
+  int unit_capacity;         // device-planned: the grid's clusters (work-list capacity)
   int batch, heads, sq, rows, page_size, kv_dtype, causal;
   int chunk_len, num_splits, max_ctx, row_blocks;
 };
@@ -47,11 +55,18 @@ struct CombineParams {
   const float* part_lse;
   uint16_t* out;
   float* lse;
+  const int4* seq_info;  // device-planned: per sequence {ctx, first partial, count, 0}
   int batch, rows, num_splits;
 };
 
 }  // namespace mla
 
 // Launchers (return a cudaError_t as int).
+extern "C" int mla_decode_epilogue(const void* ql_nope, const void* q_pe, const void* kv_c,
+                                   const void* k_pe, const int64_t* slot_mapping,
+                                   int32_t num_tokens, int32_t num_heads, void* q_out,
+                                   void* kv_cache, int64_t num_pages, int32_t page_size,
+                                   int32_t kv_dtype, const float* kv_scale,
+                                   int32_t cache_inputs_early, int32_t* status, void* stream);
 int mla_launch_fwd(const mla::FwdParams& p, void* stream);
 int mla_launch_combine(const mla::CombineParams& p, void* stream);

@@ -1,6 +1,7 @@
 // ptx.cuh -- hand-written inline-PTX wrappers for sm_103a: mbarrier,
-// cp.async, tcgen05 (TMEM alloc / MMA / commit / ld / st) and stores into
-// the shared memory of another CTA of the cluster.  Written from the
+// cp.async, tcgen05 (TMEM alloc / MMA / commit / ld / st), stores into the
+// shared memory of another CTA of the cluster and the programmatic
+// dependency wait.  Written from the
 // PTX ISA's descriptions of these instructions; no library code is used.
 #pragma once
 
@@ -293,6 +294,14 @@ __device__ __forceinline__ void st_async_u4(uint32_t cluster_addr, uint32_t a, u
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+
+// ------------------------------------------------- programmatic launch ---
+
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace ptx

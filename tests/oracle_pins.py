@@ -104,6 +104,179 @@ def pin_e4m3_spec_values(orc):
             assert got == want and math.copysign(1, got) == math.copysign(1, want), (code, got, want)
 
 
+def pin_e4m3_encode_roundtrip(orc):
+    """Every finite E4M3FN value encodes back to its own code (both zeros too)."""
+    for c in range(256):
+        v = orc.e4m3_to_double(c)
+        if math.isnan(v):
+            continue
+        assert orc.e4m3_encode(v) == c, (hex(c), v)
+
+
+def pin_e4m3_encode_matches_torch(orc):
+    """Nearest-even encoding agrees with torch's float32 -> float8_e4m3fn cast on
+    values from 1e-5 to 448 in magnitude, both signs (the cast's range)."""
+    import torch
+    g = np.random.default_rng(40)
+    x = np.concatenate([g.standard_normal(3000).astype(np.float32) * np.float32(sc)
+                        for sc in (1e-4, 1e-2, 1.0, 30.0, 200.0)])
+    x = np.clip(x, -448.0, 448.0).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(v)) for v in x], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def pin_e4m3_encode_ties_and_saturation(orc):
+    """A value halfway between two neighbouring codes takes the even one;
+    magnitudes past 448 saturate to 448; NaN stays NaN."""
+    vals = [orc.e4m3_to_double(c) for c in range(0x7F)]
+    for c in range(0x7E):
+        mid = 0.5 * (vals[c] + vals[c + 1])  # exact in binary32 (at most 5 significant bits)
+        want = c if c % 2 == 0 else c + 1
+        assert orc.e4m3_encode(mid) == want, (hex(c), mid)
+        assert orc.e4m3_encode(-mid) == 0x80 | want
+    for big in (448.5, 464.0, 480.0, 1e6, 3e38):
+        assert orc.e4m3_encode(big) == 0x7E and orc.e4m3_encode(-big) == 0xFE
+    assert orc.e4m3_encode(float("nan")) & 0x7F == 0x7F
+
+
+def _epilogue_inputs(seed, T, H, pages, ps, kv_dtype, n_pad=1):
+    g = np.random.default_rng(seed)
+    ql = rand_bits(seed + 1, (T, H, 512))
+    qp = rand_bits(seed + 2, (T, H, 64))
+    kc = rand_bits(seed + 3, (T, 512), sigma=2.0)
+    kp = rand_bits(seed + 4, (T, 64), sigma=2.0)
+    slots = g.choice(pages * ps, size=T, replace=False).astype(np.int64)
+    slots[g.choice(T, size=n_pad, replace=False)] = -1  # padding tokens
+    dt = np.uint16 if kv_dtype == syn.KV_BF16 else np.uint8
+    cache = g.integers(0, 1 << (16 if dt is np.uint16 else 8), (pages, ps, 576)).astype(dt)
+    if dt is np.uint16:
+        cache &= np.uint16(0xBFFF)  # finite patterns only
+    return ql, qp, kc, kp, slots, cache
+
+
+def pin_epilogue_bf16_concat_and_insert(orc):
+    """bf16: q rows are ql_nope then q_pe; each non-padding token's cache row
+    (page slot // ps, offset slot % ps, in a cache of random bits) becomes
+    kv_c then k_pe; every other cache element keeps its bits."""
+    T, H, P, ps = 7, 3, 5, 4
+    ql, qp, kc, kp, slots, cache = _epilogue_inputs(41, T, H, P, ps, syn.KV_BF16)
+    q, out = orc.epilogue(ql, qp, kc, kp, slots, cache, syn.KV_BF16)
+    assert np.array_equal(q[:, :, :512], ql) and np.array_equal(q[:, :, 512:], qp)
+    flat_in, flat_out = cache.reshape(-1, 576), out.reshape(-1, 576)
+    touched = np.zeros(P * ps, bool)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        touched[slots[t]] = True
+        assert np.array_equal(flat_out[slots[t], :512], kc[t])
+        assert np.array_equal(flat_out[slots[t], 512:], kp[t])
+    assert np.array_equal(flat_out[~touched], flat_in[~touched])
+
+
+def pin_epilogue_inserted_row_decodes_to_itself(orc):
+    """The decode of a one-key sequence whose key is the row the epilogue just
+    inserted returns that row's value dims and LSE = scale * <q, row>, with q
+    the concatenated query row (closed forms of the decode, bf16 and fp8)."""
+    T, H, P, ps = 3, 2, 4, 2
+    for dt, s in ((syn.KV_BF16, 1.0), (syn.KV_FP8_E4M3, 0.03125)):
+        ql, qp, kc, kp, slots, cache = _epilogue_inputs(43, T, H, P, ps, dt, n_pad=0)
+        q, out = orc.epilogue(ql, qp, kc, kp, slots, cache, dt, s)
+        for t in range(T):
+            off = int(slots[t] % ps)
+            # the inserted row, alone at offset 0 of a one-page cache
+            page = out[slots[t] // ps][off:off + 1]
+            page = np.concatenate([page, np.zeros((ps - 1, 576), page.dtype)])[None]
+            o, l = orc.decode(q[t][None, None], page, dt, s, ps, np.array([[0]], np.int32),
+                              np.array([1], np.int32), SCALE)
+            row = np.concatenate([_f(kc[t]), _f(kp[t])])
+            if dt == syn.KV_FP8_E4M3:
+                row = np.array([orc.e4m3_to_double(int(c)) * s for c in page[0, 0]])
+            assert np.array_equal(o[0, 0], np.broadcast_to(row[:512], (H, 512)))
+            qrow = np.concatenate([_f(ql[t]), _f(qp[t])], axis=1)
+            assert np.allclose(l[0, 0], SCALE * (qrow @ row), rtol=1e-12, atol=1e-12)
+
+
+def pin_epilogue_fp8_within_rounding(orc):
+    """fp8: each inserted code decodes to x / kv_scale within half an E4M3
+    spacing at that magnitude (2^-4 relative for normals, 2^-10 absolute in the
+    subnormal range), beyond 448 to 448."""
+    T, H, P, ps = 6, 1, 4, 4
+    ql, qp, kc, kp, slots, cache = _epilogue_inputs(45, T, H, P, ps, syn.KV_FP8_E4M3)
+    s = 0.0123
+    _, out = orc.epilogue(ql, qp, kc, kp, slots, cache, syn.KV_FP8_E4M3, s)
+    flat = out.reshape(-1, 576)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        x = np.concatenate([_f(kc[t]), _f(kp[t])])
+        y = (x.astype(np.float32) / np.float32(s)).astype(np.float64)
+        dec = np.array([orc.e4m3_to_double(int(c)) for c in flat[slots[t]]])
+        yc = np.clip(y, -448, 448)
+        tol = np.where(np.abs(yc) >= 2.0 ** -6, np.abs(yc) * 2.0 ** -4, 2.0 ** -10)
+        assert np.all(np.abs(dec - yc) <= tol + 1e-300)
+        assert np.all(np.sign(dec[dec != 0]) == np.sign(y[dec != 0]))
+
+
+def _kvb_weights(seed, H, sigma=1.0 / 22.6):
+    return rand_bits(seed, (H, 256, 512), sigma=sigma)
+
+
+def pin_gather_kv_matches_numpy(orc):
+    """gather_kv_b_proj against numpy's fp64 einsum over the logical rows
+    (three sequences in shuffled pages of 16, one empty): k = [W_k c, rope],
+    v = W_v c, rows packed sequence by sequence."""
+    H, lens = 3, [37, 0, 20]
+    seqs = [rand_bits(60 + b, (max(n, 1), 576))[:n] for b, n in enumerate(lens)]
+    cache, bt, sl = _pool_layout([r if len(r) else np.zeros((1, 576), np.uint16) for r in seqs],
+                                 16, seed=61)
+    sl = np.array(lens, np.int32)
+    w = _kvb_weights(62, H)
+    k, v = orc.gather_kv_b_proj(cache, syn.KV_BF16, 1.0, 16, bt, sl, w)
+    rows = np.concatenate([_f(r) for r in seqs if len(r)])
+    wf = _f(w)
+    want_k = np.einsum("hod,td->tho", wf[:, :128], rows[:, :512])
+    want_v = np.einsum("hod,td->tho", wf[:, 128:], rows[:, :512])
+    assert k.shape == (sum(lens), H, 192) and v.shape == (sum(lens), H, 128)
+    assert np.allclose(k[:, :, :128], want_k, rtol=1e-12, atol=1e-12)
+    assert np.allclose(v, want_v, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(k[:, :, 128:], np.broadcast_to(rows[:, None, 512:], (len(rows), H, 64)))
+
+
+def pin_gather_kv_selection_weights(orc):
+    """Weights that select one latent dim per output (a permutation per head,
+    times 2 for the values) give those dims exactly, fp8 cache included
+    (code * kv_scale)."""
+    H, n, ps = 2, 11, 4
+    g = np.random.default_rng(63)
+    w = np.zeros((H, 256, 512), np.uint16)
+    sel = [g.permutation(512)[:256] for _ in range(H)]
+    for h in range(H):
+        w[h, np.arange(128), sel[h][:128]] = _bf16([1.0])[0]
+        w[h, 128 + np.arange(128), sel[h][128:]] = _bf16([2.0])[0]
+    codes = g.integers(0, 0x7F, (n, 576)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11
+    cache, bt = layout(codes, ps, perm_seed=4, dtype=np.uint8)
+    s = 0.0625
+    k, v = orc.gather_kv_b_proj(cache, syn.KV_FP8_E4M3, s, ps, bt, np.array([n], np.int32), w)
+    dec = np.array([[orc.e4m3_to_double(int(c)) for c in row] for row in codes]) * s
+    for h in range(H):
+        assert np.array_equal(k[:, h, :128], dec[:, sel[h][:128]])
+        assert np.array_equal(v[:, h], 2.0 * dec[:, sel[h][128:]])
+        assert np.array_equal(k[:, h, 128:], dec[:, 512:])
+
+
+def pin_gather_kv_page_size_invariance(orc):
+    """The same logical rows at page sizes 1 and 16 expand to the same bits."""
+    rows = rand_bits(64, (50, 576))
+    w = _kvb_weights(65, 2)
+    res = []
+    for ps in (1, 16):
+        cache, bt = layout(rows, ps, perm_seed=ps)
+        res.append(orc.gather_kv_b_proj(cache, syn.KV_BF16, 1.0, ps, bt, np.array([50], np.int32), w))
+    assert np.array_equal(res[0][0], res[1][0]) and np.array_equal(res[0][1], res[1][1])
+
+
 # ---------------------------------------------------------- closed forms ---
 
 def pin_single_key(orc):

@@ -143,3 +143,54 @@ def test_fwd_rejects_bad_arguments_before_touching_the_gpu(L):
     bad = list(args)
     bad[0] = ctypes.byref(q)
     assert L.mla_decode_fwd(*bad, fake, 1 << 20, None) == mla.ERR_INVALID_ARG
+
+
+def test_epilogue_rejects_bad_arguments_before_touching_the_gpu(L):
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced
+    ok = [fake, fake, fake, fake, fake, 4, 8, fake, fake, 4, 16, 0, None, 0, None, None]
+    for i, bad in [(0, None), (4, None), (7, None), (8, None), (6, 0), (6, 129), (10, 0),
+                   (11, 2), (13, 2), (1, ctypes.c_void_p((1 << 20) + 8))]:
+        a = list(ok)
+        a[i] = bad
+        assert L.mla_decode_epilogue(*a) == mla.ERR_INVALID_ARG, i
+    a = list(ok)
+    a[11] = mla.KV_FP8_E4M3  # fp8 cache needs kv_scale
+    assert L.mla_decode_epilogue(*a) == mla.ERR_INVALID_ARG
+    a = list(ok)
+    a[5] = 0  # no tokens: nothing to queue
+    assert L.mla_decode_epilogue(*a) == mla.OK
+
+
+@pytest.mark.parametrize("b,h,sq,ps,cap,sms", [(64, 128, 1, 1, 8192, 152), (1, 16, 1, 64, 131072, 148),
+                                              (1024, 64, 2, 16, 4096, 152), (3, 128, 2, 1, 100, 8)])
+def test_dplan_info_sizes(L, b, h, sq, ps, cap, sms):
+    d = mla.dplan_info(b, h, sq, ps, 0, sq > 1, cap, sms)
+    rb = -(-(h * sq) // 128)
+    assert d.rows == h * sq and d.row_blocks == rb
+    assert d.pairs == min(sms // 2, 255) and d.max_parts == d.pairs + b
+    assert d.max_units == rb * d.max_parts
+    offs = [d.ws_units_offset, d.ws_seq_offset, d.ws_count_offset, d.ws_partial_o_offset,
+            d.ws_partial_lse_offset, d.ws_status_offset]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert d.ws_seq_offset >= d.ws_units_offset + 16 * d.max_units
+    assert d.ws_partial_lse_offset >= d.ws_partial_o_offset + 4 * d.max_parts * d.rows * 512
+    assert d.workspace_bytes >= d.ws_status_offset + 4
+
+
+def test_dplan_rejects_bad_arguments(L):
+    d = mla.DPlan()
+    for args in [(0, 16, 1, 1, 0, 0, 64, 152), (1025, 16, 1, 1, 0, 0, 64, 152),
+                 (1, 0, 1, 1, 0, 0, 64, 152), (1, 16, 1, 1, 2, 0, 64, 152),
+                 (1, 16, 1, 1, 0, 0, -1, 152)]:
+        assert L.mla_decode_dplan_info(*args, ctypes.byref(d)) == mla.ERR_INVALID_ARG
+    good = mla.dplan_info(2, 16, 1, 1, 0, False, 64, 152)
+    fake = ctypes.c_void_p(1 << 20)
+    # no workspace / too small / wrong version
+    assert L.mla_decode_plan_device(ctypes.byref(good), fake, None, None, 1 << 30, None) == mla.ERR_WORKSPACE
+    assert L.mla_decode_plan_device(ctypes.byref(good), fake, None, fake, 16, None) == mla.ERR_WORKSPACE
+    bad = mla.DPlan.from_buffer_copy(good)
+    bad.version = 7
+    assert L.mla_decode_plan_device(ctypes.byref(bad), fake, None, fake, 1 << 30, None) == mla.ERR_INVALID_ARG
+    # padded table narrower than the capacity
+    assert L.mla_decode_fwd_dplan(ctypes.byref(good), fake, fake, 8, None, fake, 32, None, 0.1, fake,
+                                  fake, fake, 1 << 30, None) == mla.ERR_INVALID_ARG

@@ -58,6 +58,23 @@ MUTATIONS = [
      "q + (((int64_t)b * H + h) * Sq + i) * ORACLE_D_QK"),
     ("row_sees_all_tokens_keys", "int64_t n = visible_keys(seq_lens[b], Sq, i, causal);",
      "int64_t n = visible_keys(seq_lens[b], Sq, Sq - 1, causal);"),
+    ("epilogue_rope_from_latent", "dst[512 + d] = q_pe[((int64_t)t * H + h) * 64 + d];",
+     "dst[512 + d] = ql_nope[((int64_t)t * H + h) * 512 + d];"),
+    ("epilogue_page_offset_swapped", "page = slot / page_size;\n      off = slot % page_size;",
+     "page = slot % page_size;\n      off = slot / page_size;"),
+    ("epilogue_scale_multiplied", "mla_oracle_bf16_to_double(x) / (double)kv_scale",
+     "mla_oracle_bf16_to_double(x) * (double)kv_scale"),
+    ("encode_ties_to_odd", "(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    ("encode_no_saturation", "if (a > 448.0) return (uint8_t)(sign | 0x7E);",
+     "if (a > 448.0) return 0x7F;"),
+    ("encode_sign_dropped", "return (uint8_t)(sign | best);", "return (uint8_t)best;"),
+    ("gkv_head_stride", "const uint16_t* w = W + ((int64_t)h * 256 + o) * 512;",
+     "const uint16_t* w = W + ((int64_t)o * H + h) * 512;"),
+    ("gkv_key_value_swapped", "if (o < 128)\n            k[", "if (o >= 128)\n            k["),
+    ("gkv_rope_from_latent", "k[(t * H + h) * 192 + 128 + d] = c[512 + d];",
+     "k[(t * H + h) * 192 + 128 + d] = c[d];"),
+    ("gkv_rows_reversed", "int64_t t = (int64_t)cu_seqlens[b] + j;",
+     "int64_t t = (int64_t)cu_seqlens[b + 1] - 1 - j;"),
 ]
 
 
