@@ -553,7 +553,7 @@ def run_epilogue_bench(args):
     mla.build()
     T, H = args.tokens or 1, args.heads or 8
     fp8 = args.kv == "fp8"
-    ps, pages = 64, max(4, (4 * T) // 64 + 4)
+    ps, pages = 64, max(4, (4 * T) // 64 + 4)  # noqa: E501
     g = np.random.default_rng(0)
     mk = lambda *sh: torch.randn(*sh, dtype=torch.float32, device="cuda").to(torch.bfloat16)  # noqa: E731
     ql, qp, kc, kp = mk(T, H, 512), mk(T, H, 64), mk(T, 512), mk(T, 64)
@@ -600,6 +600,71 @@ def run_epilogue_bench(args):
                      "frac": gbs / hbm, "bytes_per_call": moved, "peak_source": src},
         "context": {"b300_page_kernel_us": 2.06,
                     "note": "the page's fused epilogue on B300, Kimi-K3 TP8 decode at concurrency 1"},
+        "gpu_launches": steps}))
+    return 0
+
+
+def run_gather_kvb_bench(args):
+    """The cached-prefix expansion alone (gather_kv_b_proj): the pages' shape,
+    12 TP8-local heads, fp8 cache at page size 1, one sequence of --ctx cached
+    tokens (default 32000); µs per call, TB/s moved and TFLOP/s against the
+    measured peaks.  Synthetic kv_b_proj weights ~ N(0, 1/512)."""
+    import torch
+    import paged_mla_decode_latent_gb300 as mla
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity import to_device
+    torch.cuda.set_device(0)
+    mla.build()
+    H = args.heads or 12
+    batch = args.batch or 1
+    ctx = args.ctx or 32000
+    fp8 = args.kv != "bf16"
+    p = syn.make_problem(batch, 1, 4, [ctx] * batch, 1, syn.KV_FP8_E4M3 if fp8 else syn.KV_BF16,
+                         False, seed=0, name=f"gather_kvb_h{H}_b{batch}_ctx{ctx}")
+    t = to_device(p)
+    w = (torch.randn((H, 256, 512), device="cuda") / math.sqrt(512.0)).to(torch.bfloat16)
+    cu = torch.arange(batch + 1, dtype=torch.int32, device="cuda") * ctx
+    T = batch * ctx
+    k = torch.empty((T, H, 192), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((T, H, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    call = lambda: mla.gather_kv_b_proj(t["cache"], t["scale"], t["bt"], t["lens"], cu, ctx, w, k,  # noqa: E731
+                                        v, status, stream)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"status {int(status.item()):#x}")
+    steps = args.steps if args.steps > 0 else 50
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    row = 576 if fp8 else 1152
+    moved = T * row + T * H * (192 + 128) * 2 + H * 256 * 512 * 2 + batch * 8
+    flops = 2.0 * T * H * 256 * 512
+    hbm, tc, _, src = load_peaks()
+    t_hbm, t_tc = moved / (hbm * 1e9), flops / (tc * 1e12)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    achieved = flops / (us * 1e-6) / 1e12 if bound == "tensor" else moved / (us * 1e-6) / 1e9
+    peak = tc if bound == "tensor" else hbm
+    print(json.dumps({
+        "metric": "gather_kv_b_proj µs/call (cached-prefix K/V expansion)", "value": us,
+        "unit": "us", "higher_is_better": False, "steps": steps, "n_gpus": 1,
+        "dtype": "fp8_e4m3->bf16" if fp8 else "bf16",
+        "config": {"workload": p.name, "heads": H, "batch": batch, "ctx": ctx, "page_size": 1},
+        "tb_per_s": moved / (us * 1e-6) / 1e12,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s" if bound == "tensor" else "GB/s", "frac": achieved / peak,
+                     "roofline_us": max(t_hbm, t_tc) * 1e6, "bytes_per_call": moved,
+                     "flops_per_call": flops, "peak_source": src},
+        "context": {"mi355x_page_ms": {"4096": 0.038, "32000": 0.227, "65536": 0.442,
+                                       "109440": 0.711},
+                    "note": "the page's Triton kernel on MI355X (Kimi-K3 TP8, 12 heads, fp8, ps 1)"},
         "gpu_launches": steps}))
     return 0
 
@@ -658,10 +723,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense",
-                    choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp", "epilogue"])
+                    choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp", "epilogue",
+                             "gather_kvb"])
     ap.add_argument("--tokens", type=int, default=0, help="epilogue workload: tokens (default 1)")
     ap.add_argument("--heads", type=int, default=0, help="epilogue workload: heads (default 8)")
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="epilogue workload: cache")
+    ap.add_argument("--kv", default="", choices=["", "bf16", "fp8"],
+                    help="epilogue (default bf16) / gather_kvb (default fp8) workload: cache")
     ap.add_argument("--batch", type=int, default=0, help="dense workload: batch (default 64)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="dense (default 8192) or fp8_long (default 109440) workload: context")
@@ -682,6 +749,8 @@ def main(argv=None):
         return run_launch_check(args)
     if args.workload == "epilogue":
         return run_epilogue_bench(args)
+    if args.workload == "gather_kvb":
+        return run_gather_kvb_bench(args)
     if args.impl == "reference":
         if args.steps <= 0:
             args.steps = 3
