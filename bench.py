@@ -48,7 +48,8 @@ MI355X_HK_US = {"dense": 132.878}  # the pages' HK m16x8 time for this workload 
 
 # ------------------------------------------------------------------ workload ---
 
-def make_workload(name: str, seed: int = 0, batch: int = 0, ctx: int = 0) -> syn.Problem:
+def make_workload(name: str, seed: int = 0, batch: int = 0, ctx: int = 0, heads: int = 0,
+                  sq: int = 0, page_size: int = 0) -> syn.Problem:
     if name == "dense":
         return syn.dense(batch or 64, ctx or 8192, seed=seed)
     if name == "ragged_bf16":
@@ -58,7 +59,7 @@ def make_workload(name: str, seed: int = 0, batch: int = 0, ctx: int = 0) -> syn
     if name == "fp8_long":
         return syn.fp8_long(ctx or 109440, seed=seed)
     if name == "mtp":
-        return syn.mtp(64, 2, 1, seed=seed)
+        return syn.mtp(heads or 64, sq or 2, page_size or 1, seed=seed)
     raise ValueError(name)
 
 
@@ -211,7 +212,8 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    p = make_workload(args.workload, batch=args.batch, ctx=args.ctx)
+    p = make_workload(args.workload, batch=args.batch, ctx=args.ctx, heads=args.heads, sq=args.sq,
+                      page_size=args.page_size)
     import oracle
     oracle.build()
     per_step = []
@@ -267,7 +269,8 @@ def run_gpu(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     mla.build()
-    p = make_workload(args.workload, seed=rank, batch=args.batch, ctx=args.ctx)
+    p = make_workload(args.workload, seed=rank, batch=args.batch, ctx=args.ctx, heads=args.heads,
+                      sq=args.sq, page_size=args.page_size)
     alg = algorithmic(p)
     t = to_device(p, dev)
     out = torch.empty((p.batch, p.sq, p.heads, 512), dtype=torch.bfloat16, device=dev)
@@ -726,7 +729,10 @@ def main(argv=None):
                     choices=["dense", "ragged_bf16", "ragged_fp8", "fp8_long", "mtp", "epilogue",
                              "gather_kvb"])
     ap.add_argument("--tokens", type=int, default=0, help="epilogue workload: tokens (default 1)")
-    ap.add_argument("--heads", type=int, default=0, help="epilogue workload: heads (default 8)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="epilogue (default 8), gather_kvb (12) or mtp (64) workload: heads")
+    ap.add_argument("--sq", type=int, default=0, help="mtp workload: query tokens (default 2)")
+    ap.add_argument("--page-size", type=int, default=0, help="mtp workload: page size (default 1)")
     ap.add_argument("--kv", default="", choices=["", "bf16", "fp8"],
                     help="epilogue (default bf16) / gather_kvb (default fp8) workload: cache")
     ap.add_argument("--batch", type=int, default=0, help="dense workload: batch (default 64)")

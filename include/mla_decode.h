@@ -106,7 +106,8 @@ typedef struct mla_decode_plan_t {
   int32_t row_tile;     /* rows one CTA pair handles (128) */
   int32_t row_blocks;   /* ceil(rows / row_tile) */
   int32_t max_ctx;      /* longest context the plan covers */
-  int32_t key_tile;     /* keys per pipeline stage (64) */
+  int32_t key_tile;     /* keys per pipeline tile: 128 when rows <= 64 (bf16) or <= 16
+                           (fp8), the few-row kernel; 64 otherwise */
   int32_t chunk_len;    /* keys per split, a multiple of key_tile */
   int32_t num_splits;   /* splits per sequence = ceil(max_ctx / chunk_len) */
   int32_t num_sms;      /* SM count the partition was balanced for */
@@ -137,7 +138,7 @@ typedef struct mla_decode_plan_t {
  * num_sms        SMs to balance for; 0 queries the current device
  * plan           host out-parameter
  *
- * The chunk length is a multiple of the 64-key tile, chosen by simulating
+ * The chunk length is a multiple of the key tile, chosen by simulating
  * the in-order block dispatch over the SMs for each candidate split count
  * and keeping the fastest (partial-output traffic counted).  The plan stays
  * valid for later calls whose contexts are all <= plan->max_ctx; splits past
@@ -222,10 +223,10 @@ int mla_decode_check(const mla_decode_plan_t* plan, const void* workspace, void*
  * Nothing queued depends on the lengths' values, so a CUDA graph of the last
  * three calls stays valid whatever the lengths become, up to ctx_capacity.
  * The partition: with P = num_sms / 2 pairs and K = the batch's 64-key tiles,
- * sequences are cut into chunks of max(ceil(K / P), 2) tiles unless none is
- * longer than 5/4 of that share (then none is cut); units are listed chunk
- * level by chunk level, sequences with more chunks first.  At most P + B
- * chunks, so max_units = row_blocks * (P + B).
+ * sequences are cut into chunks of max(ceil(ceil(K / P) / 2), 2) tiles unless
+ * none is longer than 5/4 of the share ceil(K / P) (then none is cut); units
+ * are listed chunk level by chunk level, sequences with more chunks first.
+ * At most 2P + B chunks, so max_units = row_blocks * (2P + B).
  *
  * Page tables: the padded block table of mla_decode_fwd (kv_indptr NULL), or
  * the CSR form: kv_indptr device int32 [B + 1], sequence b's page ids are
@@ -240,11 +241,13 @@ typedef struct mla_decode_dplan_t {
   int32_t row_blocks;     /* ceil(rows / 128) */
   int32_t ctx_capacity;   /* longest context any call may bring */
   int32_t num_sms;        /* SMs the partition is balanced for */
-  int32_t pairs;          /* P = num_sms / 2 (at most 255) */
-  int32_t max_parts;      /* partial-slot capacity, P + B */
-  int32_t max_units;      /* work-list capacity and launch size, row_blocks * (P + B) */
-  int32_t min_chunk_keys; /* shortest chunk a cut sequence gets (128) */
+  int32_t pairs;          /* P = num_sms / 2 (at most 127) */
+  int32_t max_parts;      /* partial-slot capacity, 2P + B */
+  int32_t max_units;      /* work-list capacity and launch size, row_blocks * (2P + B) */
+  int32_t min_chunk_keys; /* shortest chunk a cut sequence gets (2 key tiles) */
+  int32_t key_tile;       /* 64, or 128 for the few-row kernel (as mla_decode_plan_t) */
   int32_t wait_limit_us;  /* as in mla_decode_plan_t: 0 = 2 s; the one field a caller may set */
+  int32_t reserved0;
   int64_t ws_units_offset;  /* int32x4 [max_units] {b, row block | chunk << 8, k0, k1} */
   int64_t ws_seq_offset;    /* int32x4 [B] {clamped ctx, first partial slot, chunks, 0} */
   int64_t ws_count_offset;  /* int32 [4] {units, chunk keys, partial slots used, 0} */

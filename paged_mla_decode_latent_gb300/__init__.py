@@ -67,7 +67,7 @@ class DPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "batch", "num_heads", "sq", "page_size", "kv_dtype", "causal", "rows",
         "row_blocks", "ctx_capacity", "num_sms", "pairs", "max_parts", "max_units",
-        "min_chunk_keys", "wait_limit_us")] + [
+        "min_chunk_keys", "key_tile", "wait_limit_us", "reserved0")] + [
         (n, ctypes.c_int64) for n in (
             "ws_units_offset", "ws_seq_offset", "ws_count_offset", "ws_partial_o_offset",
             "ws_partial_lse_offset", "ws_status_offset", "workspace_bytes")]

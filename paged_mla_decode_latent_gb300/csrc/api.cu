@@ -27,6 +27,11 @@ int check_plan(const mla_decode_plan_t* plan) {
   if (plan->kv_dtype != MLA_KV_BF16 && plan->kv_dtype != MLA_KV_FP8_E4M3)
     return MLA_ERR_INVALID_ARG;
   if (plan->wait_limit_us < 0) return MLA_ERR_INVALID_ARG;
+  if (plan->key_tile != mla::kKeyTile && plan->key_tile != mla::kKeyTileSmall)
+    return MLA_ERR_INVALID_ARG;
+  if (plan->key_tile == mla::kKeyTileSmall && !mla_small_rows_fit(plan->rows, plan->kv_dtype))
+    return MLA_ERR_INVALID_ARG;
+  if (plan->chunk_len % plan->key_tile != 0) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 
@@ -81,6 +86,7 @@ int fwd_impl(const mla_decode_plan_t* plan, const void* q, const void* kv_cache,
   p.seq_info = nullptr;
   p.bt_indptr = nullptr;
   p.unit_capacity = 0;
+  p.key_tile = plan->key_tile;
   p.batch = plan->batch;
   p.heads = plan->num_heads;
   p.sq = plan->sq;
@@ -196,5 +202,6 @@ cudaError_t opt_in_smem(const void* kernel, int bytes, int dev, int slot) {
 }  // namespace mla
 
 int mla_launch_fwd(const mla::FwdParams& p, void* stream) {
+  if (p.key_tile == mla::kKeyTileSmall) return mla_launch_fwd_small_sm103(p, stream);
   return mla_launch_fwd_sm103(p, stream);
 }

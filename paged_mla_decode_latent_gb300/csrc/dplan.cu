@@ -16,12 +16,15 @@
 // description: size the grid from the valid tokens, not kv_indices'
 // capacity) use.
 //
-// The partition: with P = num_sms / 2 CTA pairs and K = sum of ceil(ctx/64)
-// key tiles over the batch, every sequence is cut into chunks of
-// max(ceil(K / P), 2) tiles, unless no sequence is longer than 5/4 of that
-// fair share, in which case none is cut (measured on the host-planned
-// kernel: cutting batch 64 x 8192 into 113 + 15 tiles was slower than whole
-// sequences).  So at most P + B chunks exist, each a unit per 128-row block.
+// The partition: with P = num_sms / 2 CTA pairs and K = sum of ceil(ctx/T)
+// key tiles over the batch (T = 64, or 128 for the few-row kernel) (the fair share of a pair is ceil(K / P) tiles),
+// every sequence is cut into chunks of max(ceil(share / 2), 2) tiles, unless
+// no sequence is longer than 5/4 of the share, in which case none is cut
+// (measured on the host-planned kernel: cutting batch 64 x 8192 into 113 +
+// 15 tiles was slower than whole sequences).  Half the share keeps the
+// greedy dispatch within 1.5 shares of the ideal and matches the host
+// planner's simulated choice on the ragged batch (84-tile chunks there, 78
+// here).  So at most 2P + B chunks exist, each a unit per 128-row block.
 // Units are listed chunk by chunk (all first chunks, then all second ...),
 // sequences with more chunks first, which is the longest-first order that
 // list scheduling of the in-order block dispatch favours.  A sequence in one
@@ -40,8 +43,7 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kMaxDplanBatch = 1024;
-constexpr int kMaxChunksPerSeq = mla::kMaxSplits;  // chunks of one sequence: at most P <= 255
-constexpr int kTileKeys = 64;
+constexpr int kMaxChunksPerSeq = mla::kMaxSplits;  // chunks of one sequence: at most 2P <= 254
 constexpr int kMinChunkTiles = 2;
 
 int64_t align256(int64_t a) { return (a + 255) / 256 * 256; }
@@ -53,7 +55,7 @@ struct PlanArgs {
   int4* seq_info;
   int32_t* counts;  // [0] units, [1] chunk keys, [2] partial slots
   int32_t* status;
-  int batch, row_blocks, pairs, page_size, ctx_capacity, max_units;
+  int batch, row_blocks, pairs, page_size, ctx_capacity, max_units, tile_keys;
 };
 
 __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(PlanArgs a) {
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(PlanArgs a) {
       ctx = ctx < 0 ? 0 : (int)cap;
     }
     s_ctx[b] = ctx;
-    const int t = (ctx + kTileKeys - 1) / kTileKeys;
+    const int t = (ctx + a.tile_keys - 1) / a.tile_keys;
     tiles += t;
     max_t = max(max_t, t);
   }
@@ -105,9 +107,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(PlanArgs a) {
       mx = max(mx, s_redi[w]);
     }
     const long long fair = (total + a.pairs - 1) / a.pairs;
-    long long chunk = mx <= fair + fair / 4 ? mx : (fair > kMinChunkTiles ? fair : kMinChunkTiles);
+    const long long half = (fair + 1) / 2;
+    long long chunk = mx <= fair + fair / 4 ? mx : (half > kMinChunkTiles ? half : kMinChunkTiles);
     if (chunk < 1) chunk = 1;
-    s_chunk = (int)chunk * kTileKeys;
+    s_chunk = (int)chunk * a.tile_keys;
   }
   __syncthreads();
   const int chunk_keys = s_chunk;
@@ -167,6 +170,8 @@ int check_dplan(const mla_decode_dplan_t* d) {
     return MLA_ERR_INVALID_ARG;
   if (d->pairs < 1 || d->max_units < 1 || d->max_parts < 1 || d->wait_limit_us < 0)
     return MLA_ERR_INVALID_ARG;
+  if (d->key_tile != (mla_small_rows_fit(d->rows, d->kv_dtype) ? mla::kKeyTileSmall : mla::kKeyTile))
+    return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 
@@ -214,10 +219,12 @@ extern "C" int mla_decode_dplan_info(int32_t batch, int32_t num_heads, int32_t s
   d.ctx_capacity = ctx_capacity;
   d.num_sms = num_sms;
   d.pairs = num_sms / mla::kClusterSize < 1 ? 1 : num_sms / mla::kClusterSize;
-  if (d.pairs > kMaxChunksPerSeq - 1) d.pairs = kMaxChunksPerSeq - 1;
-  d.max_parts = d.pairs + batch;
+  // a cut sequence has at most 2P chunks, which the merge holds in shared memory
+  if (2 * d.pairs > kMaxChunksPerSeq - 1) d.pairs = (kMaxChunksPerSeq - 1) / 2;
+  d.max_parts = 2 * d.pairs + batch;
   d.max_units = d.row_blocks * d.max_parts;
-  d.min_chunk_keys = kMinChunkTiles * kTileKeys;
+  d.key_tile = mla_small_rows_fit(d.rows, kv_dtype) ? mla::kKeyTileSmall : mla::kKeyTile;
+  d.min_chunk_keys = kMinChunkTiles * d.key_tile;
   int64_t off = 0;
   d.ws_units_offset = off;
   off = align256(off + (int64_t)d.max_units * 16);
@@ -257,6 +264,7 @@ extern "C" int mla_decode_plan_device(const mla_decode_dplan_t* dplan, const int
   a.page_size = dplan->page_size;
   a.ctx_capacity = dplan->ctx_capacity;
   a.max_units = dplan->max_units;
+  a.tile_keys = dplan->key_tile;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The status word is reset here, before the planning kernel, so that only
   // kernels sit between the planner, the decode and the merge.
@@ -330,6 +338,7 @@ extern "C" int mla_decode_fwd_dplan(const mla_decode_dplan_t* dplan, const void*
   p.num_splits = 1;
   p.max_ctx = dplan->ctx_capacity;
   p.row_blocks = dplan->row_blocks;
+  p.key_tile = dplan->key_tile;
   if (mla_launch_fwd(p, stream) != 0) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -12,6 +12,7 @@ constexpr int kDQK = 576;       // query/key row: 512 latent + 64 rope
 constexpr int kDV = 512;        // value: first 512 dims of the same row
 constexpr int kRowTile = 128;   // score rows per CTA pair (the MMA M)
 constexpr int kKeyTile = 64;    // keys per pipeline stage (the QK^T MMA N)
+constexpr int kKeyTileSmall = 128;  // the same for the few-row kernel
 constexpr int kClusterSize = 2; // CTAs per work unit: each owns half the value dims
 constexpr int kMaxRows = 1024;  // H * Sq limit
 constexpr int kMaxSplits = 256; // split-count cap of the planner
@@ -41,6 +42,7 @@ struct FwdParams {
   const int4* seq_info;
   const int32_t* bt_indptr;  // CSR row starts into bt (kv_indices), or nullptr
   int unit_capacity;         // device-planned: the grid's clusters (work-list capacity)
+  int key_tile;              // 64: the 128-row kernel; 128: the few-row kernel
   int batch, heads, sq, rows, page_size, kv_dtype, causal;
   int chunk_len, num_splits, max_ctx, row_blocks;
 };
@@ -60,6 +62,11 @@ struct CombineParams {
 };
 
 }  // namespace mla
+
+// The few-row kernel (128-key tiles) takes problems of at most this many
+// score rows per sequence: 64 with a bf16 cache, 16 with fp8.
+bool mla_small_rows_fit(int rows, int kv_dtype);
+int mla_launch_fwd_small_sm103(const mla::FwdParams& p, void* stream);
 
 // Launchers (return a cudaError_t as int).
 extern "C" int mla_decode_epilogue(const void* ql_nope, const void* q_pe, const void* kv_c,

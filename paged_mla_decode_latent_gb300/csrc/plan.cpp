@@ -99,7 +99,9 @@ extern "C" int mla_decode_plan(const int32_t* seq_lens_host, int32_t batch, int3
   p.row_tile = mla::kRowTile;
   p.row_blocks = (int32_t)ceil_div(p.rows, p.row_tile);
   p.max_ctx = max_ctx;
-  p.key_tile = mla::kKeyTile;
+  // Few rows per sequence run on the 128-key-tile kernel (its chunks are
+  // multiples of 128 keys); everything else on the 128-row, 64-key one.
+  p.key_tile = mla_small_rows_fit(p.rows, kv_dtype) ? mla::kKeyTileSmall : mla::kKeyTile;
   p.num_sms = num_sms;
   p.cluster_size = mla::kClusterSize;
 

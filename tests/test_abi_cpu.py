@@ -167,7 +167,7 @@ def test_dplan_info_sizes(L, b, h, sq, ps, cap, sms):
     d = mla.dplan_info(b, h, sq, ps, 0, sq > 1, cap, sms)
     rb = -(-(h * sq) // 128)
     assert d.rows == h * sq and d.row_blocks == rb
-    assert d.pairs == min(sms // 2, 255) and d.max_parts == d.pairs + b
+    assert d.pairs == min(sms // 2, 127) and d.max_parts == 2 * d.pairs + b
     assert d.max_units == rb * d.max_parts
     offs = [d.ws_units_offset, d.ws_seq_offset, d.ws_count_offset, d.ws_partial_o_offset,
             d.ws_partial_lse_offset, d.ws_status_offset]

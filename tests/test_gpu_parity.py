@@ -102,6 +102,28 @@ def test_split_count_invariance():
         assert_close(o, l, outs[0][1], outs[0][2], "split vs split")
 
 
+@pytest.mark.parametrize("kv_dtype,heads,sq", [(syn.KV_FP8_E4M3, 16, 1), (syn.KV_BF16, 16, 4),
+                                               (syn.KV_BF16, 64, 1)])
+def test_split_count_invariance_few_rows(kv_dtype, heads, sq):
+    """The 128-key-tile kernel (at most 64 rows bf16, 16 fp8) over 1 to many splits."""
+    p = syn.make_problem(2, sq, heads, [3001, 2500], 16, kv_dtype, sq > 1, seed=41, name="few_rows")
+    ref_o, ref_l = oracle_full(p)
+    splits = set()
+    for num_sms in (2, 8, 148, 4000):
+        out, lse, plan, st = run_gpu(p, num_sms=num_sms)
+        assert plan.key_tile == 128 and st == 0
+        assert_close(out, lse, ref_o, ref_l, f"num_sms={num_sms} splits={plan.num_splits}")
+        splits.add(plan.num_splits)
+    assert len(splits) >= 3
+
+
+@pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
+def test_rescale_while_earlier_pv_in_flight_few_rows(kv_dtype):
+    p = _growing_rope(kv_dtype, [0.2, 0.2, 6.0, 6.0, 12.0, 12.0, 18.0, 18.0, 24.0, 24.0, 1.0, 1.0],
+                      heads=16)
+    check(p)
+
+
 @pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
 def test_cuda_graph_replay_matches_eager(kv_dtype):
     """fwd + combine captured into one CUDA graph (the combine's programmatic
