@@ -414,14 +414,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const char* cache = static_cast<const char*>(p.cache);
     const int n_halves = 2 * n_tiles;
     const int lw = loader_index(warp);
-    // i-th key of this lane in half u, clamped to the split's last key: a
-    // partial half, or the empty second half of an odd last tile, repeats a
-    // real row (its weights are masked to zero), so no stage slot the value
-    // MMA reads holds anything but cache rows.
-    auto key_of = [&](int u, int i) -> int {
-      const int start = k0 + u * HALF;
-      return start + min(i * IPI + g, max(0, min(HALF, k1 - start)) - 1);
-    };
+    // i-th key of this lane in half u, clamped to the split's last key k1 - 1:
+    // a partial half, or the empty second half of a split's last tile,
+    // repeats a real row (its weights are masked to zero), so every key read
+    // lies in [k0, k1) and no stage slot the value MMA reads holds anything
+    // but cache rows.
+    auto key_of = [&](int u, int i) -> int { return min(k0 + u * HALF + i * IPI + g, k1 - 1); };
     const uint32_t pdiv = (uint32_t)p.page_size;
     const uint32_t plog = 32u - __clz(pdiv - 1u);
     const uint32_t pmul = (uint32_t)(((1ull << 32) * ((1ull << plog) - pdiv)) / pdiv) + 1u;

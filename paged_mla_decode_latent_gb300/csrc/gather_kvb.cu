@@ -14,19 +14,19 @@
 // chunk storing its own slice.
 //
 // GB300 form: a CTA takes 128 tokens of one sequence (the MMA M) and a group
-// of up to kGroup heads.  The 128 gathered latent rows stay in shared memory
-// for the whole group as the A operand (K-major, 128B-swizzled, 8 slabs of 64
-// dims; fp8 codes converted to bf16 on the way in, exactly).  Each head's
-// 256 x 512 weight block streams through a ring of 64-dim slabs (the B
-// operand, 256 rows N); tcgen05 MMAs (M = 128, N = 256, K = 16) accumulate
-// one head in 256 TMEM columns while four epilogue warps drain the previous
-// head from the other 256 (fp32 -> bf16, x kv_scale for fp8).
+// of up to kGroup heads.  The 128 gathered latent rows go into TMEM as the A
+// operand (256 columns of bf16 pairs; fp8 codes converted exactly on the
+// way), so shared memory holds only the weights: each (head, key or value
+// half) unit's 128 x 512 block streams through a ring of twelve 64-dim
+// slabs (16 KB each, the B operand, K-major 128B-swizzled), about 192 KB in
+// flight.  tcgen05 MMAs (M = 128, N = 128, K = 16, A from TMEM) accumulate a
+// unit in one of two 128-column TMEM accumulators while four epilogue warps
+// drain the other (fp32 -> bf16, x kv_scale for fp8).
 //
-// Warps: 0-2 weight loaders (one per ring stage), 3 MMA issue, 4-7 epilogue
-// (TMEM lane quarters 0-3); the MMA and epilogue warps gather the latent
-// rows first while the loaders start on the weights.  Every wait is
-// bounded (2 s): a wait that runs out sets MLA_DEVFLAG_TIMEOUT and the CTA
-// winds down.
+// Warps: 0-2 weight loaders (each keeps four slabs in flight), 3 MMA issue,
+// 4-7 gather the rows into TMEM, write the rope dims and drain the
+// accumulators (TMEM lane quarters 0-3).  Every wait is bounded (2 s): a
+// wait that runs out sets MLA_DEVFLAG_TIMEOUT and the CTA winds down.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,36 +40,35 @@
 namespace {
 
 constexpr int kTok = 128;           // tokens per CTA (MMA M)
-constexpr int kN = 256;             // outputs per head (MMA N): 128 key + 128 value
+constexpr int kUnitN = 128;         // outputs per unit (MMA N): a head's keys or its values
 constexpr int kLatent = 512;        // contraction (MMA K over 8 slabs)
 constexpr int kSlabs = kLatent / 64;
 constexpr int kGroup = 16;          // heads per CTA (the gathered rows serve them all)
-constexpr int kStages = 3;          // weight slabs in flight
-constexpr int A_SLAB = kTok * 128;  // 16 KB
-constexpr int B_SLAB = kN * 128;    // 32 KB
-constexpr int OFF_A = 0;
-constexpr int OFF_B = kSlabs * A_SLAB;           // 128 KB
-constexpr int OFF_BAR = OFF_B + kStages * B_SLAB;  // 224 KB
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr int kLoaders = 3;
+constexpr int kInFlight = 4;        // slabs a loader warp keeps in flight
+constexpr int kStages = kLoaders * kInFlight;  // 12
+constexpr int B_SLAB = kUnitN * 128;           // 16 KB
+constexpr int OFF_B = 0;
+constexpr int OFF_BAR = OFF_B + kStages * B_SLAB;  // 192 KB
+constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
 static_assert(SMEM_BYTES <= 232448, "smem");
-constexpr int kLoaders = kStages;  // weight loader warps, one per ring stage
-constexpr int kWarps = kLoaders + 1 + 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kMmaWarp = kLoaders;
-constexpr int kGatherThreads = kThreads - 32 * kLoaders;  // MMA + epilogue warps gather A
+constexpr int kMmaWarp = 3;
+constexpr int kThreads = 32 * 8;
+constexpr uint32_t TM_A = 0;    // 256 columns: the 512 latent dims as bf16 pairs
+constexpr uint32_t TM_D = 256;  // two 128-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Bars {
-  uint64_t a_full;           // latent rows gathered (all threads)
-  uint64_t b_full[kStages];  // weight slab landed (its loader warp's 32 lanes)
-  uint64_t b_empty[kStages]; // weight slab consumed (MMA commit)
-  uint64_t d_full[2];        // a head's accumulator complete (MMA commit)
-  uint64_t d_empty[2];       // accumulator drained (128 epilogue threads)
+  uint64_t a_full;            // rows in TMEM (128 gather threads)
+  uint64_t b_full[kStages];   // weight slab landed (its loader warp's 32 lanes)
+  uint64_t b_empty[kStages];  // weight slab consumed (MMA commit)
+  uint64_t d_full[2];         // a unit's accumulator complete (MMA commit)
+  uint64_t d_empty[2];        // accumulator drained (128 epilogue threads)
   uint64_t drain;
   uint32_t tmem_base;
   int32_t abort;
 };
-static_assert(sizeof(Bars) <= 256, "barriers");
+static_assert(sizeof(Bars) <= 512, "barriers");
 
 struct GkvParams {
   const void* cache;
@@ -146,11 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
   const int n_tok = min(kTok, ctx - j0);
   const int h0 = group * kGroup;
   const int n_heads = min(kGroup, p.heads - h0);
+  const int n_units = 2 * n_heads;  // (head, keys or values)
+  const int n_slabs = n_units * kSlabs;
   const int64_t t0 = (int64_t)p.cu_seqlens[b] + j0;
   const float s_kv = p.fp8 && p.kv_scale ? *p.kv_scale : 1.f;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&bars.a_full), kGatherThreads);
+    ptx::mbar_init(ptx::smem_u32(&bars.a_full), 128);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars.b_full[s]), 32);
       ptx::mbar_init(ptx::smem_u32(&bars.b_empty[s]), 1);
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
     }
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
     bars.abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    ptx::fence_mbar_init_cluster();
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars.tmem_base), 512);
@@ -173,117 +174,68 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort};
 
-  const int n_slabs = n_heads * kSlabs;
-  if (warp >= kMmaWarp) {
-    // ---- MMA and epilogue warps: gather the chunk's latent rows into A ----
-    // A piece is 16 bytes of bf16 operand (8 dims), 64 per row, stored
-    // 128B-swizzled in its 64-dim slab.  bf16: 16-byte cp.async copies, all
-    // in flight at once.  fp8: 8 codes per piece loaded in batches of 8 and
-    // converted (exactly) by the loading thread.  Rows past the sequence are
-    // zero (their outputs are not stored).
-    const int gt = threadIdx.x - 32 * kMmaWarp;
-    const char* cache = static_cast<const char*>(p.cache);
-    const int32_t* bt = p.bt + (size_t)b * p.bt_stride;
-    bool bad = false;
-    auto row_of = [&](int r) -> int64_t {
-      const int j = j0 + r;
-      int64_t page = bt[j / p.page_size];
-      if (page < 0 || page >= p.num_pages) {
-        bad = true;
-        page = 0;
-      }
-      return page * p.page_size + j % p.page_size;
-    };
-    auto dst_of = [&](int i) -> uint32_t {
-      const int r = i >> 6, piece = i & 63;
-      return sbase + OFF_A + (piece >> 3) * A_SLAB + r * 128 + (((piece & 7) ^ (r & 7)) * 16);
-    };
-    auto zero = [&](uint32_t dst) {
-      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
-    };
-    constexpr int kPieces = kTok * 64;
-    if (!p.fp8) {
-      for (int i = gt; i < kPieces; i += kGatherThreads) {
-        const int r = i >> 6;
-        if (r < n_tok)
-          ptx::cp_async_16(dst_of(i), cache + (row_of(r) * MLA_D_QK + (i & 63) * 8) * 2);
-        else
-          zero(dst_of(i));
-      }
-      ptx::cp_async_commit();
-      ptx::cp_async_wait<0>();
-    } else {
-      for (int i0 = gt; i0 < kPieces; i0 += 8 * kGatherThreads) {
-        uint2 codes[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * kGatherThreads, r = i >> 6;
-          codes[u] = (i < kPieces && r < n_tok)
-                         ? *reinterpret_cast<const uint2*>(cache + row_of(r) * MLA_D_QK + (i & 63) * 8)
-                         : make_uint2(0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * kGatherThreads;
-          if (i >= kPieces) break;
-          const uint32_t x = e4m3x2_to_bf16x2(codes[u].x), y = e4m3x2_to_bf16x2(codes[u].x >> 16);
-          const uint32_t z = e4m3x2_to_bf16x2(codes[u].y), w = e4m3x2_to_bf16x2(codes[u].y >> 16);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst_of(i)), "r"(x),
-                       "r"(y), "r"(z), "r"(w)
-                       : "memory");
-        }
-      }
-    }
-    if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(ptx::smem_u32(&bars.a_full));
-  }
-
   if (warp < kLoaders) {
     // ------------------------------------------------- weight loaders ---
-    // Loader warp w owns ring stage w and fills slabs w, w + kStages, ...:
-    // 256 rows x 128 B of one head's block, 16-byte pieces into the
-    // 128B-swizzled K-major layout; it waits for its own copies, fences them
-    // for the tensor cores and arrives on the stage's barrier.
-    for (int i = warp; i < n_slabs; i += kStages) {
-      const int s = warp;
-      if (i >= kStages && !wait_all(c, ptx::smem_u32(&bars.b_empty[s]), ((i / kStages) - 1) & 1))
+    // Loader warp w fills slabs i = w, w + 3, ... (slab k = i % 8 of unit
+    // i / 8: 128 weight rows x 64 dims) into stage i % 12, which it owns:
+    // 16-byte cp.async pieces into the 128B-swizzled K-major layout, one
+    // commit group per slab, four groups in flight; when a group is done the
+    // lanes fence it for the tensor cores and arrive on its stage's barrier.
+    int pend[kInFlight];
+    int n_pend = 0, head = 0;
+    bool ok = true;
+    for (int i = warp; i < n_slabs; i += kLoaders) {
+      const int s = i % kStages;
+      if (i >= kStages && !wait_all(c, ptx::smem_u32(&bars.b_empty[s]), ((i / kStages) - 1) & 1)) {
+        ok = false;
         break;
-      const int h = h0 + i / kSlabs, k = i % kSlabs;
-      const uint16_t* src = p.w + ((size_t)h * kN) * kLatent + k * 64;
+      }
+      const int unit = i / kSlabs, k = i % kSlabs;
+      const int h = h0 + (unit >> 1), x = unit & 1;
+      const uint16_t* src = p.w + ((size_t)h * 256 + x * kUnitN) * kLatent + k * 64;
       const uint32_t dst = sbase + OFF_B + s * B_SLAB;
 #pragma unroll 4
-      for (int q = lane; q < kN * 8; q += 32) {
+      for (int q = lane; q < kUnitN * 8; q += 32) {
         const int o = q >> 3, piece = q & 7;
         ptx::cp_async_16(dst + o * 128 + ((piece ^ (o & 7)) * 16), src + (size_t)o * kLatent + piece * 8);
       }
       ptx::cp_async_commit();
-      ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_u32(&bars.b_full[s]));
+      pend[(head + n_pend) % kInFlight] = s;
+      if (++n_pend == kInFlight) {
+        ptx::cp_async_wait<kInFlight - 1>();
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(ptx::smem_u32(&bars.b_full[pend[head]]));
+        head = (head + 1) % kInFlight;
+        --n_pend;
+      }
     }
     ptx::cp_async_wait<0>();
+    if (ok) {
+      ptx::fence_proxy_async_smem();
+      for (; n_pend > 0; --n_pend, head = (head + 1) % kInFlight)
+        ptx::mbar_arrive(ptx::smem_u32(&bars.b_full[pend[head]]));
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA ---
     if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_f16(128, kN, 1u, false, false);
+      const uint32_t idesc = ptx::idesc_f16(128, kUnitN, 1u, false, false);
       bool ok = wait(c, ptx::smem_u32(&bars.a_full), 0);
       ptx::tc_fence_after();
-      for (int hh = 0; ok && hh < n_heads; ++hh) {
-        const int buf = hh & 1;
-        if (hh >= 2 && !wait(c, ptx::smem_u32(&bars.d_empty[buf]), ((hh >> 1) - 1) & 1)) break;
+      for (int uu = 0; ok && uu < n_units; ++uu) {
+        const int buf = uu & 1;
+        if (uu >= 2 && !wait(c, ptx::smem_u32(&bars.d_empty[buf]), ((uu >> 1) - 1) & 1)) break;
         ptx::tc_fence_after();
-        const uint32_t d = tmem + buf * kN;
+        const uint32_t d = tmem + TM_D + buf * kUnitN;
         for (int k = 0; k < kSlabs; ++k) {
-          const int i = hh * kSlabs + k, s = i % kStages;
+          const int i = uu * kSlabs + k, s = i % kStages;
           if (!wait(c, ptx::smem_u32(&bars.b_full[s]), (i / kStages) & 1)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a = sbase + OFF_A + k * A_SLAB, bb = sbase + OFF_B + s * B_SLAB;
+          const uint32_t bb = sbase + OFF_B + s * B_SLAB;
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ss(d, kdesc(a + kk * 32), kdesc(bb + kk * 32), idesc, (k | kk) != 0);
+            ptx::mma_ts(d, tmem + TM_A + k * 32 + kk * 8, kdesc(bb + kk * 32), idesc, (k | kk) != 0);
           ptx::mma_commit(ptx::smem_u32(&bars.b_empty[s]));
         }
         if (!ok) break;
@@ -292,21 +244,63 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
     }
     __syncwarp();
   } else {
-    // -------------------------------------------------------- epilogue ---
-    // Thread i of epilogue warp w owns TMEM lane 32 (w % 4) + i, i.e. token
-    // row r of the chunk; it writes that token's rope dims once per head,
-    // then each head's 128 key and 128 value dims.
-    const int q4 = warp & 3;  // warps 4-7: lane quarters 0-3
+    // ------------------------------------------- gather and epilogue ---
+    // Thread i of warp w (4..7) owns TMEM lane 32 (w % 4) + i, i.e. token row
+    // r of the chunk.
+    const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const bool valid = r < n_tok;
     const int64_t t = t0 + r;
+    const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
+    const char* cache = static_cast<const char*>(p.cache);
+    int64_t row = 0;
     if (valid) {
       const int j = j0 + r;
       int64_t page = p.bt[(size_t)b * p.bt_stride + j / p.page_size];
-      if (page < 0 || page >= p.num_pages) page = 0;
-      const int64_t row = page * p.page_size + j % p.page_size;
+      if (page < 0 || page >= p.num_pages) {
+        atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
+        page = 0;
+      }
+      row = page * p.page_size + j % p.page_size;
+    }
+    // The row's 512 latent dims -> TMEM (columns = dims / 2), 128 dims a batch.
+    for (int bq = 0; bq < 4; ++bq) {
+      uint32_t w[64];
+      if (!p.fp8) {
+        const uint4* src = reinterpret_cast<const uint4*>(cache + (row * MLA_D_QK + bq * 128) * 2);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint4 x = valid ? src[v] : make_uint4(0, 0, 0, 0);
+          w[4 * v] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(cache + row * MLA_D_QK + bq * 128);
+        uint4 x[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) x[v] = valid ? src[v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t cw[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            w[8 * v + 2 * e] = e4m3x2_to_bf16x2(cw[e]);
+            w[8 * v + 2 * e + 1] = e4m3x2_to_bf16x2(cw[e] >> 16);
+          }
+        }
+      }
+      ptx::tmem_st32(tmem + lanes + TM_A + bq * 64, *reinterpret_cast<uint32_t(*)[32]>(w));
+      ptx::tmem_st32(tmem + lanes + TM_A + bq * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
+    }
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(ptx::smem_u32(&bars.a_full));
+
+    // The rope dims, once per head of the group.
+    if (valid) {
       uint4 rope[8];
-      const char* cache = static_cast<const char*>(p.cache);
       if (p.fp8) {
         const uint4* src = reinterpret_cast<const uint4*>(cache + row * MLA_D_QK + 512);
         for (int v = 0; v < 4; ++v) {
@@ -332,29 +326,28 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
         for (int v = 0; v < 8; ++v) dst[v] = rope[v];
       }
     }
-    const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
-    for (int hh = 0; hh < n_heads; ++hh) {
-      const int buf = hh & 1;
-      if (!wait_all(c, ptx::smem_u32(&bars.d_full[buf]), (hh >> 1) & 1)) break;
+    // Drain each unit: keys to k[t, h, 0:128], values to v[t, h, 0:128].
+    for (int uu = 0; uu < n_units; ++uu) {
+      const int buf = uu & 1;
+      if (!wait_all(c, ptx::smem_u32(&bars.d_full[buf]), (uu >> 1) & 1)) break;
       ptx::tc_fence_after();
-      const int h = h0 + hh;
+      const int h = h0 + (uu >> 1);
+      uint16_t* dst = buf == 0 ? p.k_out + (t * p.heads + h) * 192 : p.v_out + (t * p.heads + h) * 128;
 #pragma unroll 1
-      for (int part = 0; part < kN / 32; ++part) {
+      for (int part = 0; part < kUnitN / 32; ++part) {
         uint32_t x[32];
-        ptx::tmem_ld32(tmem + lanes + buf * kN + part * 32, x);
+        ptx::tmem_ld32(tmem + lanes + TM_D + buf * kUnitN + part * 32, x);
         ptx::tmem_ld_wait();
         if (valid) {
-          uint16_t* dst = part < 4 ? p.k_out + (t * p.heads + h) * 192 + part * 32
-                                   : p.v_out + (t * p.heads + h) * 128 + (part - 4) * 32;
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + part * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+            uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16(__uint_as_float(x[8 * v + 2 * e]) * s_kv,
+              o[e] = pack_bf16(__uint_as_float(x[8 * v + 2 * e]) * s_kv,
                                __uint_as_float(x[8 * v + 2 * e + 1]) * s_kv);
-            d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[v] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }

@@ -255,6 +255,22 @@ def test_wait_limit_runs_out_without_fault():
     assert_close(out2, lse2, ref_o, ref_l, "after a timed-out call")
 
 
+@pytest.mark.parametrize("heads", [16, 128])
+def test_fp8_query_range_edges(heads):
+    """With an fp8 cache the kernels stage q as f16: q scaled by 2^-10 (many
+    elements in f16's subnormal range) still meets the tolerance, and one
+    element past 65504 sets MLA_DEVFLAG_Q_RANGE."""
+    p = syn.make_problem(2, 1, heads, [700, 130], 16, syn.KV_FP8_E4M3, False, seed=44,
+                         name="q_small")
+    x = syn.bf16_bits_to_f32(p.q_bits) * np.float32(2.0 ** -10)
+    p.q_bits = syn.f32_to_bf16_bits(x)
+    check(p)
+    big = syn.make_problem(1, 1, heads, [300], 16, syn.KV_FP8_E4M3, False, seed=45, name="q_big")
+    big.q_bits[0, 0, 3, 17] = syn.f32_to_bf16_bits(np.array([70000.0], np.float32))[0]
+    _, _, _, status = run_gpu(big)
+    assert status & mla.DEVFLAG_Q_RANGE
+
+
 def test_run_to_run_determinism():
     p = syn.dense(2, 1500, seed=17)
     t = to_device(p)
