@@ -394,10 +394,11 @@ def run_gpu(args):
         roof["peak_sustained"] = tc_sus
         roof["frac_sustained"] = achieved / tc_sus
     prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
+    if os.path.exists(prof) and not args.dplan:
         try:
             tr = json.load(open(prof)).get(args.workload)
-            if tr and tr.get("kernel_rev") == kernel_revision():
+            if (tr and tr.get("kernel_rev") == kernel_revision(tr.get("sources"))
+                    and tr.get("alg_bytes_per_launch") == alg["bytes"]):
                 roof["traffic"] = tr["dram_bytes_per_launch"]
         except Exception:
             pass
@@ -672,12 +673,13 @@ def run_gather_kvb_bench(args):
     return 0
 
 
-def kernel_revision() -> str:
-    """Hash of the kernel sources: traffic figures are void once it changes."""
+def kernel_revision(sources=None) -> str:
+    """Hash of the sources that define a kernel (default: all of csrc/): a
+    recorded traffic figure is void once any of them changes."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_mla_decode_latent_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(sources or os.listdir(csrc)):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 

@@ -63,28 +63,40 @@ constexpr int STAGE = 4 * ATOM + RATOM; // 72 KB
 constexpr int NS = 2;                   // operand stages (one tile each)
 constexpr int RAW_HALF = HALF * (256 + 32);  // fp8 codes of a half: 18 KB
 constexpr int NR = 3;                   // raw slots (one per loader warp)
-// Warps: with at most 64 rows only TMEM lanes 0..63 hold rows, i.e. lane
-// quarters 0 and 1, which warps 0, 1, 4 and 5 reach (a warp reaches quarter
-// warp % 4): those are the softmax warps, 16 rows each.  Warps 2, 3 and 6
-// load, warp 7 issues the MMAs.  Eight warps leave 255 registers a thread.
+// Rows and warps: a warp reaches only the TMEM lane quarter warp % 4, and
+// each quarter belongs to one SM sub-partition.  So that all four
+// sub-partitions share the softmax, the (at most 64) rows are spread 16 to a
+// quarter: row 16 q + i of the problem is row 32 q + i of the MMA's A and of
+// every accumulator (lanes 32 q + 16 .. 32 q + 31 hold unused rows).  Warp q
+// (0..3) is the softmax warp of quarter q; warps 4-6 load, warp 7 issues the
+// MMAs.  Eight warps leave 255 registers a thread.
 constexpr int kLoaders = 3;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 7;
 constexpr int kThreads = 32 * 8;
-__device__ __forceinline__ bool is_softmax_warp(int w) { return (w & 2) == 0 && w != kMmaWarp; }
-__device__ __forceinline__ int loader_index(int w) { return w == 6 ? 2 : w - 2; }  // warps 2, 3, 6
+__device__ __forceinline__ bool is_softmax_warp(int w) { return w < kSoftmaxWarps; }
+__device__ __forceinline__ int loader_index(int w) { return w - kSoftmaxWarps; }  // warps 4, 5, 6
+__device__ __forceinline__ int mma_row(int r) { return 32 * (r >> 4) + (r & 15); }
 constexpr int RECV_W = 32 * 16 * 12;    // one warp's partial scores: 16 rows x 128 keys x 3 B (6 KB)
 
 template <bool kFp8>
 struct Layout {
-  // Q slabs sized for the padded rows (a multiple of 16, at most 64);
-  // the MMA's A reads run past them into the stages (rows never used).
-  __host__ __device__ static constexpr int qslab(int rpad) { return rpad * 128; }
-  __host__ __device__ static constexpr int qbytes(int rpad) { return 4 * rpad * 128 + rpad * 64; }
+  // Q as the A operand (128 MMA rows, K-major; the MMA reads all 128 rows of
+  // a slab, 16 KB, and the unused ones may hold anything).  bf16 (up to 64
+  // rows, at MMA rows 32 q + i): the real rows of a latent slab are its
+  // 8-row groups 4q and 4q + 1, so slabs 2k and 2k + 1 interleave 2 KB
+  // apart in one 16 KB span (each one's unused groups are the other's rows):
+  // 32 KB of latent slabs, then the rope slab (64-byte rows, 8 KB).  fp8 (up
+  // to 16 rows, MMA rows 0..15): slabs of 16 rows packed 2 KB apart, their
+  // unused rows reading into the stages, then the rope rows (1 KB).
+  __host__ __device__ static constexpr int qslab_off(int a) {
+    return kFp8 ? a * 2048 : (a >> 1) * 16384 + (a & 1) * 2048;
+  }
+  __host__ __device__ static constexpr int qrope_off() { return kFp8 ? 4 * 2048 : 2 * 16384; }
+  __host__ __device__ static constexpr int qbytes() { return kFp8 ? 4 * 2048 + 1024 : 2 * 16384 + 8192; }
   static constexpr int max_rows = kFp8 ? 16 : 64;
   static constexpr int OFF_Q = 0;
-  // room for max_rows rows of Q, 1 KB aligned (36 KB for bf16, 9 KB for fp8)
-  static constexpr int OFF_STAGE = (qbytes(max_rows) + 1023) / 1024 * 1024;
+  static constexpr int OFF_STAGE = (qbytes() + 1023) / 1024 * 1024;  // 40 KB bf16, 9 KB fp8
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_RECV = OFF_RAW + (kFp8 ? NR * RAW_HALF : 0);
   static constexpr int RECV = (max_rows / 16) * RECV_W;
@@ -246,7 +258,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int rpad = (p.rows + 15) & ~15;
 
   // The work unit (as in the 128-row kernel; rows fit one block here).
   int b, ctx, k0, k1;
@@ -325,8 +336,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::grid_dependency_wait();
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort, p.wait_ns};
-  const uint32_t q_slab = (uint32_t)L::qslab(rpad);  // bytes between Q's latent slabs
-  const uint32_t q_rope = 4 * q_slab;                // Q's rope half (64-byte rows)
 
   if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -341,10 +350,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + L::OFF_STAGE + (u % NS) * STAGE;
         for (int a = 0; a < 4; ++a)
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ss(d, kdesc128(qa + a * q_slab + kk * 32), kdesc128(st + a * ATOM + kk * 32),
-                        id_qk, (a | kk) != 0);
+            ptx::mma_ss(d, kdesc128(qa + L::qslab_off(a) + kk * 32),
+                        kdesc128(st + a * ATOM + kk * 32), id_qk, (a | kk) != 0);
         for (int kk = 0; kk < 2; ++kk)  // this CTA's 32 rope dims
-          ptx::mma_ss(d, kdesc64(qa + q_rope + kk * 32), kdesc64(st + 4 * ATOM + kk * 32), id_qk, 1);
+          ptx::mma_ss(d, kdesc64(qa + L::qrope_off() + kk * 32), kdesc64(st + 4 * ATOM + kk * 32),
+                      id_qk, 1);
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
       };
       auto issue_pv = [&](int t, bool second) {
@@ -530,17 +540,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cp_async_wait<0>();
   } else {
     // ----------------------------------------------------------- softmax ---
-    // As in the 128-row kernel: the warp owns TMEM lanes lbase .. lbase + 15,
-    // lbase = 32 (warp % 4) + 16 (warp / 4); thread i holds rows
-    // rA = lbase + i/4, rB = rA + 8 and, of every 8-key group j of the 128
-    // keys, keys 8j + 2(i%4), 8j + 2(i%4) + 1.  Only warps whose rows hold
-    // real rows work; the others keep the barrier phases moving.
-    const int q4 = warp & 3;                  // lane quarter 0 or 1
-    const int g = warp >> 2;                  // which 16-lane half of it
-    const int sw = q4 | (g << 1);             // softmax warp index 0..3
-    const int lbase = q4 * 32 + g * 16;
+    // As in the 128-row kernel's 16x256b access: warp q owns TMEM lanes
+    // 32 q .. 32 q + 15 (problem rows 16 q .. 16 q + 15); thread i holds
+    // lanes 32 q + i/4 and + 8 (rows rA = 16 q + i/4, rB = rA + 8) and, of
+    // every 8-key group j of the 128 keys, keys 8j + 2(i%4), 8j + 2(i%4) + 1.
+    // Only warps whose rows are real work; the others keep the barrier
+    // phases moving.
+    const int q4 = warp;
+    const int sw = q4;
+    const int lbase = q4 * 32;
     const int cq = lane & 3;
-    const int rA = lbase + (lane >> 2), rB = rA + 8;
+    const int rA = 16 * q4 + (lane >> 2), rB = rA + 8;  // problem rows
     const uint32_t lanes16 = (uint32_t)lbase << 16;
     auto visible = [&](int r) {
       if (r >= p.rows) return 0;
@@ -550,26 +560,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return min(nvis, k1);
     };
     const int visA = visible(rA), visB = visible(rB);
-    const bool live = lbase < p.rows;
+    const bool live = 16 * q4 < p.rows;
 
     // Q -> shared memory: this CTA's 256 latent dims (4 slabs, 128B swizzle)
-    // and its 32 rope dims (64B swizzle), rows padded with zeros to rpad.
+    // and its 32 rope dims (64B swizzle), problem row r at MMA row
+    // mma_row(r).
     {
       bool q_range = false;
-      const int n_pieces = rpad * 36;  // per row: 4 slabs x 8 chunks + 4 rope chunks
+      const int n_pieces = p.rows * 36;  // per row: 4 slabs x 8 chunks + 4 rope chunks
       for (int i = sw * 32 + lane; i < n_pieces; i += 32 * kSoftmaxWarps) {
-        const int r = i / 36, pc = i % 36;
-        uint4 x = make_uint4(0, 0, 0, 0);
+        const int r = i / 36, pc = i % 36, ar = mma_row(r);
         const uint16_t* qrow = p.q + ((size_t)b * p.rows + r) * mla::kDQK;
+        uint4 x;
         uint32_t dst;
         if (pc < 32) {
           const int sl = pc >> 3, ch = pc & 7;
-          if (r < p.rows) x = reinterpret_cast<const uint4*>(qrow + vdim0 + sl * 64)[ch];
-          dst = sbase + L::OFF_Q + sl * q_slab + sw128(r, ch);
+          x = reinterpret_cast<const uint4*>(qrow + vdim0 + sl * 64)[ch];
+          dst = sbase + L::OFF_Q + L::qslab_off(sl) + sw128(ar, ch);
         } else {
           const int ch = pc - 32;
-          if (r < p.rows) x = reinterpret_cast<const uint4*>(qrow + 512 + 32 * (int)rank)[ch];
-          dst = sbase + L::OFF_Q + q_rope + sw64(r, ch);
+          x = reinterpret_cast<const uint4*>(qrow + 512 + 32 * (int)rank)[ch];
+          dst = sbase + L::OFF_Q + L::qrope_off() + sw64(ar, ch);
         }
         if (kFp8) x = bf16x8_to_f16x8(x, q_range);
         st_shared_u4(dst, x);
@@ -582,7 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
     float mA = kMaxSentinel, mB = kMaxSentinel;
     float lA = 0.f, lB = 0.f;
-    const int slot = lbase >> 4;  // receive slot of this warp's rows
+    const int slot = q4;  // receive slot of this warp's rows
     const uint32_t my_recv = sbase + L::OFF_RECV + slot * RECV_W;
     const uint32_t peer_recv = ptx::mapa(my_recv, peer);
     const uint32_t peer_free = ptx::mapa(sbase + L::OFF_XFREE + sw * 4, peer);
@@ -602,13 +613,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // s[32 hf + 4 j + e]: key half hf (keys 64 hf ..), 8-key group j;
       // e = 0, 1 -> row A keys 8j + 2cq + e; e = 2, 3 -> row B
       float s[64];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t raw[32];
-        ptx::tmem_ld16x256b_x8(scol + hf * 64, raw);
+      {
+        uint32_t raw[2][32];
+        ptx::tmem_ld16x256b_x8(scol, raw[0]);
+        ptx::tmem_ld16x256b_x8(scol + 64, raw[1]);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * hf + i] = __uint_as_float(raw[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(raw[0][i]);
+          s[32 + i] = __uint_as_float(raw[1][i]);
+        }
       }
       // Swap partial scores with the same warp of the partner CTA (single
       // receive buffer: tile t goes once the partner has read tile t - 1).
@@ -778,7 +792,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const float invA = lA > 0.f ? s_kv / lA : 0.f, invB = lB > 0.f ? s_kv / lB : 0.f;
       const bool okA = rA < p.rows, okB = rB < p.rows;
-      const size_t pA = part * p.rows + rA;
+      const size_t pA = part * p.rows + rA;  // problem rows (TMEM lanes are spread)
       const size_t pB = part * p.rows + rB;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {

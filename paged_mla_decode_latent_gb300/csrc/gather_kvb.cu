@@ -49,7 +49,9 @@ constexpr int kInFlight = 4;        // slabs a loader warp keeps in flight
 constexpr int kStages = kLoaders * kInFlight;  // 12
 constexpr int B_SLAB = kUnitN * 128;           // 16 KB
 constexpr int OFF_B = 0;
-constexpr int OFF_BAR = OFF_B + kStages * B_SLAB;  // 192 KB
+constexpr int STG_W = 32 * 256;                    // a warp's 32 output rows of 256 B
+constexpr int OFF_STG = OFF_B + kStages * B_SLAB;  // 192 KB: output staging, 4 x 8 KB
+constexpr int OFF_BAR = OFF_STG + 4 * STG_W;       // 224 KB
 constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
 static_assert(SMEM_BYTES <= 232448, "smem");
 constexpr int kMmaWarp = 3;
@@ -250,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const bool valid = r < n_tok;
-    const int64_t t = t0 + r;
     const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
     const char* cache = static_cast<const char*>(p.cache);
     int64_t row = 0;
@@ -298,32 +299,42 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
     ptx::tc_fence_before();
     ptx::mbar_arrive(ptx::smem_u32(&bars.a_full));
 
-    // The rope dims, once per head of the group.
-    if (valid) {
-      uint4 rope[8];
-      if (p.fp8) {
-        const uint4* src = reinterpret_cast<const uint4*>(cache + row * MLA_D_QK + 512);
-        for (int v = 0; v < 4; ++v) {
-          const uint4 x = src[v];
-          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-          uint32_t o8[8];
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t bf0 = e4m3x2_to_bf16x2(w4[e]), bf1 = e4m3x2_to_bf16x2(w4[e] >> 16);
-            o8[2 * e] = pack_bf16(__uint_as_float(bf0 << 16) * s_kv,
+    // Output rows are H * 384 B (keys) or H * 256 B (values) apart, so a
+    // thread writing its own token's row would touch 32 lines per warp
+    // store.  Instead the warp's 32 rows go through its staging tile (8 KB,
+    // 16-byte chunks swizzled by the row) and leave as whole rows: lanes
+    // 16 k .. 16 k + 15 write 16 bytes each of one row, two rows per store.
+    const uint32_t stg = sbase + OFF_STG + q4 * STG_W;
+    const int half = lane >> 4, cl = lane & 15;
+    // The rope dims, once per head: 8 lanes per 128-byte rope row, 4 rows a
+    // store, each chunk read once from the cache and written for every head.
+    {
+      const int c8 = lane & 7;
+      for (int it = 0; it < 8; ++it) {
+        const int rr = q4 * 32 + it * 4 + (lane >> 3);
+        if (rr >= n_tok) continue;
+        const int j = j0 + rr;
+        int64_t page = p.bt[(size_t)b * p.bt_stride + j / p.page_size];
+        if (page < 0 || page >= p.num_pages) page = 0;
+        const int64_t crow = page * p.page_size + j % p.page_size;
+        uint4 v;
+        if (p.fp8) {
+          const uint2 codes = *reinterpret_cast<const uint2*>(cache + crow * MLA_D_QK + 512 + c8 * 8);
+          const uint32_t cw[2] = {codes.x, codes.y};
+          uint32_t o4[4];
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t bf0 = e4m3x2_to_bf16x2(cw[e]), bf1 = e4m3x2_to_bf16x2(cw[e] >> 16);
+            o4[2 * e] = pack_bf16(__uint_as_float(bf0 << 16) * s_kv,
                                   __uint_as_float(bf0 & 0xFFFF0000u) * s_kv);
-            o8[2 * e + 1] = pack_bf16(__uint_as_float(bf1 << 16) * s_kv,
+            o4[2 * e + 1] = pack_bf16(__uint_as_float(bf1 << 16) * s_kv,
                                       __uint_as_float(bf1 & 0xFFFF0000u) * s_kv);
           }
-          rope[2 * v] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-          rope[2 * v + 1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+          v = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        } else {
+          v = *reinterpret_cast<const uint4*>(cache + (crow * MLA_D_QK + 512 + c8 * 8) * 2);
         }
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(cache + (row * MLA_D_QK + 512) * 2);
-        for (int v = 0; v < 8; ++v) rope[v] = src[v];
-      }
-      for (int hh = 0; hh < n_heads; ++hh) {
-        uint4* dst = reinterpret_cast<uint4*>(p.k_out + (t * p.heads + h0 + hh) * 192 + 128);
-        for (int v = 0; v < 8; ++v) dst[v] = rope[v];
+        for (int hh = 0; hh < n_heads; ++hh)
+          *reinterpret_cast<uint4*>(p.k_out + ((t0 + rr) * p.heads + h0 + hh) * 192 + 128 + c8 * 8) = v;
       }
     }
     // Drain each unit: keys to k[t, h, 0:128], values to v[t, h, 0:128].
@@ -332,27 +343,48 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
       if (!wait_all(c, ptx::smem_u32(&bars.d_full[buf]), (uu >> 1) & 1)) break;
       ptx::tc_fence_after();
       const int h = h0 + (uu >> 1);
-      uint16_t* dst = buf == 0 ? p.k_out + (t * p.heads + h) * 192 : p.v_out + (t * p.heads + h) * 128;
-#pragma unroll 1
+      // All four 32-column loads in flight before one wait.
+      uint32_t x[4][32];
+#pragma unroll
+      for (int part = 0; part < kUnitN / 32; ++part)
+        ptx::tmem_ld32(tmem + lanes + TM_D + buf * kUnitN + part * 32, x[part]);
+      ptx::tmem_ld_wait();
+#pragma unroll
       for (int part = 0; part < kUnitN / 32; ++part) {
-        uint32_t x[32];
-        ptx::tmem_ld32(tmem + lanes + TM_D + buf * kUnitN + part * 32, x);
-        ptx::tmem_ld_wait();
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + part * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t o[4];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              o[e] = pack_bf16(__uint_as_float(x[8 * v + 2 * e]) * s_kv,
-                               __uint_as_float(x[8 * v + 2 * e + 1]) * s_kv);
-            d4[v] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack_bf16(__uint_as_float(x[part][8 * v + 2 * e]) * s_kv,
+                             __uint_as_float(x[part][8 * v + 2 * e + 1]) * s_kv);
+          const int chunk = part * 4 + v;  // 16-byte chunk of this row (0..15)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           stg + lane * 256 + ((chunk ^ (lane & 15)) * 16)),
+                       "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                       : "memory");
         }
       }
+      // The accumulator is read: the MMAs may reuse it while the rows leave.
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bars.d_empty[buf]));
+      __syncwarp();
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int lr = 2 * k + half;  // the warp's row
+        const int rr = q4 * 32 + lr;
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(stg + lr * 256 + ((cl ^ (lr & 15)) * 16))
+                     : "memory");
+        if (rr < n_tok) {
+          uint16_t* dst = buf == 0 ? p.k_out + ((t0 + rr) * p.heads + h) * 192
+                                   : p.v_out + ((t0 + rr) * p.heads + h) * 128;
+          reinterpret_cast<uint4*>(dst)[cl] = v;
+        }
+      }
+      __syncwarp();
     }
   }
 
