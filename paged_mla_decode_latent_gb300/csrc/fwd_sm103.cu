@@ -674,11 +674,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    auto recv_add = [&](int t, float (&s)[32]) -> bool {
+    auto load_scores = [&](int t, uint32_t (&raw)[32]) {
+      ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_S + (t & 1) * T, raw);
+      ptx::tmem_ld_wait();
+    };
+    // Wait for the partner's block of tile t.  With two receive buffers the
+    // warp meanwhile watches for its own scores of tile t + 1 and sends them
+    // the moment they exist (next_sent), so that transfer overlaps the rest
+    // of this wait and the softmax of tile t.
+    auto await_block = [&](int t, bool& next_sent) -> bool {
       const int rbuf = t % NRECV;
       const uint32_t rf = ptx::smem_u32(&bars.recv_full[rbuf][sw]);
+      const uint32_t par = (t / NRECV) & 1;
       if (lane == 0) ptx::mbar_arrive_expect_tx(rf, RECV_W);
-      if (!wait_all(c, rf, (t / NRECV) & 1)) return false;
+      if (NRECV == 1 || next_sent) return wait_all(c, rf, par);
+      const uint32_t sn = ptx::smem_u32(&bars.s_full[(t + 1) & 1]);
+      const uint32_t sn_par = ((t + 1) >> 1) & 1;
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (true) {
+        if (!next_sent && __all_sync(0xffffffffu, ptx::mbar_test_wait(sn, sn_par))) {
+          uint32_t raw[32];
+          ptx::tc_fence_after();
+          load_scores(t + 1, raw);
+          if (!send_tile(t + 1, raw)) return false;
+          next_sent = true;
+          return wait_all(c, rf, par);
+        }
+        if (__all_sync(0xffffffffu, ptx::mbar_test_wait(rf, par))) return true;
+        if (*c.abort) return false;
+        if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
+          atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
+          *c.abort = 1;
+          return false;
+        }
+        __nanosleep(64);
+      }
+    };
+    // Add the partner's block of tile t (complete) to this warp's partial scores.
+    auto add_block = [&](int t, float (&s)[32]) {
+      const int rbuf = t % NRECV;
       const uint32_t src = recv_addr(rbuf) + lane * 16;
       uint32_t fold = 0;
 #pragma unroll
@@ -708,11 +742,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::st_async_b32(ptx::mapa(sbase + L::OFF_XFREE + (rbuf * 8 + sw) * 4, peer),
                           any ? 1u : 0u,
                           ptx::mapa(ptx::smem_u32(&bars.recv_free[rbuf][sw]), peer));
-      return true;
-    };
-    auto load_scores = [&](int t, uint32_t (&raw)[32]) {
-      ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_S + (t & 1) * T, raw);
-      ptx::tmem_ld_wait();
     };
     // A warp whose 16 rows are all past the problem's rows (fewer than 128
     // rows) swaps nothing and computes nothing; it only keeps the barrier
@@ -720,15 +749,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // garbage that no output reads (the MMAs keep rows apart).
     const bool live = rb * mla::kRowTile + lbase < p.rows;
     bool ok = true;
-    if (NRECV == 2 && live) {  // tile 0 goes out first
-      uint32_t raw[32];
-      ok = wait_all(c, ptx::smem_u32(&bars.s_full[0]), 0);
-      if (ok) {
-        ptx::tc_fence_after();
-        load_scores(0, raw);
-        ok = send_tile(0, raw);
-      }
-    }
+    bool next_sent = false;  // two buffers: tile t + 1 already sent while waiting on tile t
     for (int t = 0; ok && t < n_tiles; ++t) {
       const int buf = t & 1;
       if (!wait_all(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
@@ -744,18 +765,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         load_scores(t, raw);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
-        if (NRECV == 1 && !send_tile(t, raw)) { ok = false; break; }
+        // this tile's block, unless it went out during the previous wait
+        const bool sent = NRECV == 2 && next_sent;
+        next_sent = false;
+        if (!sent && !send_tile(t, raw)) { ok = false; break; }
       }
-      if (!recv_add(t, s)) { ok = false; break; }
-      if (NRECV == 2 && t + 1 < n_tiles) {
-        // Scores of tile t + 1 out now: QK^T of tile t + 1 went into the
-        // other score buffer once PV of tile t - 1 was issued.
-        uint32_t raw[32];
-        if (!wait_all(c, ptx::smem_u32(&bars.s_full[buf ^ 1]), ((t + 1) >> 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        load_scores(t + 1, raw);
-        if (!send_tile(t + 1, raw)) { ok = false; break; }
-      }
+      if (t + 1 >= n_tiles) next_sent = true;  // nothing to send ahead
+      if (!await_block(t, next_sent)) { ok = false; break; }
+      add_block(t, s);
       // Row maxima over the visible keys of this tile (log2 domain).  Only the
       // last tile of a split and causal rows need the mask.
       const int tile0 = k0 + t * T;
