@@ -75,7 +75,9 @@ constexpr int QROPE = 128 * 128;       // rope dims of Q, 128 rows x 128 B
 // rounded to 24 bits (16 significant bits) and packed four to three words.
 constexpr int kSoftmaxWarps = 8;
 constexpr int RECV_W = 32 * 32 * 3;                  // one warp's block (3 KB)
-constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (24 KB)
+constexpr int RECV = kSoftmaxWarps * RECV_W;         // one tile (24 KB), one buffer
+constexpr int X_FREE = RECV;                         // [8] words the "buffer free" signals land in
+constexpr int XCHG = X_FREE + 128;
 // Warps: 0..2 loaders (warp w owns operand stage w), 3 MMA, 4..11 softmax;
 // 12 warps leave 168 registers a thread.
 constexpr int kSoftmaxWarp0 = 4;
@@ -95,13 +97,8 @@ struct Layout {
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_QROPE = OFF_RAW + NR * RAW_STAGE;
-  // Receive buffers of the score exchange: two with a bf16 cache (a warp
-  // sends tile t + 1 before it works on tile t), one with fp8 (no room),
-  // then [2][8] words the "buffer read" signals land in.
-  static constexpr int NRECV = kFp8 ? 1 : 2;
   static constexpr int OFF_RECV = OFF_QROPE + QROPE;
-  static constexpr int OFF_XFREE = OFF_RECV + NRECV * RECV;
-  static constexpr int OFF_BAR = OFF_XFREE + 128;
+  static constexpr int OFF_BAR = OFF_RECV + XCHG;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers + alignment slack
 };
 static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
@@ -124,8 +121,8 @@ struct Bars {
   uint64_t kv_empty[4];   // operand stage consumed by the MMAs
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t recv_full[2][kSoftmaxWarps];  // the partner warp's partial scores landed (3 KB)
-  uint64_t recv_free[2][kSoftmaxWarps];  // the partner warp has read what this warp sent
+  uint64_t recv_full[kSoftmaxWarps];  // the partner warp's partial scores landed (3 KB)
+  uint64_t recv_free[kSoftmaxWarps];  // the partner warp has read what this warp sent
   uint64_t o_done;
   uint64_t o_final;  // the last PV has drained (one phase)
   uint64_t q_ready;
@@ -205,6 +202,9 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return r;
 }
 
+// fp32 bits + half a unit of the 24-bit value: the top three bytes are the
+// value rounded to 16 significant bits (half away from zero on the magnitude).
+__device__ __forceinline__ uint32_t round_up_bits(float x) { return __float_as_uint(x) + 0x80u; }
 
 // Four values -> three words (the upper three bytes of each).
 __device__ __forceinline__ void pack24(uint32_t A, uint32_t B, uint32_t C, uint32_t D, uint32_t* w) {
@@ -347,11 +347,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * kSoftmaxWarps);
     }
-    for (int i = 0; i < 2; ++i)
-      for (int w = 0; w < kSoftmaxWarps; ++w) {
-        ptx::mbar_init(ptx::smem_u32(&bars.recv_full[i][w]), 1);
-        ptx::mbar_init(ptx::smem_u32(&bars.recv_free[i][w]), 1);
-      }
+    for (int w = 0; w < kSoftmaxWarps; ++w) {
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_full[w]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.recv_free[w]), 1);
+    }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.o_final), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * kSoftmaxWarps);
@@ -644,113 +643,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
     float mA = kMaxSentinel, mB = kMaxSentinel;  // running maxima (log2 domain), quad-uniform
     float lA = 0.f, lB = 0.f;                     // exact row sums over this thread's keys
-    // The score exchange with the same warp of the partner CTA.  Tile u
-    // goes into the partner's receive buffer u % NRECV once the partner has
-    // read tile u - NRECV from it.  With two buffers (bf16) a warp sends tile
-    // t + 1 as soon as its scores exist, before it works on tile t, so the
-    // transfer runs under that work instead of in front of it.
-    constexpr int NRECV = L::NRECV;
-    auto recv_addr = [&](int rbuf) { return sbase + OFF_RECV + rbuf * RECV + sw * RECV_W; };
-    auto send_tile = [&](int u, const uint32_t (&raw)[32]) -> bool {
-      const int rbuf = u % NRECV;
-      if (u >= NRECV) {
-        const uint32_t fr = ptx::smem_u32(&bars.recv_free[rbuf][sw]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fr, 4);
-        if (!wait_all(c, fr, ((u / NRECV) - 1) & 1)) return false;
-      }
-      const uint32_t dst = ptx::mapa(recv_addr(rbuf), peer) + lane * 16;
-      const uint32_t bar = ptx::mapa(ptx::smem_u32(&bars.recv_full[rbuf][sw]), peer);
-#pragma unroll
-      for (int qd = 0; qd < 2; ++qd) {  // 16 scores -> 12 words -> 3 stores
-        uint32_t w[12];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // rounded to 24 bits: the top 3 bytes of x + 0x80
-          pack24(raw[16 * qd + 4 * k] + 0x80u, raw[16 * qd + 4 * k + 1] + 0x80u,
-                 raw[16 * qd + 4 * k + 2] + 0x80u, raw[16 * qd + 4 * k + 3] + 0x80u, w + 3 * k);
-#pragma unroll
-        for (int v = 0; v < 3; ++v)
-          ptx::st_async_u4(dst + (3 * qd + v) * 512, w[4 * v], w[4 * v + 1], w[4 * v + 2],
-                           w[4 * v + 3], bar);
-      }
-      return true;
-    };
-    auto load_scores = [&](int t, uint32_t (&raw)[32]) {
-      ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_S + (t & 1) * T, raw);
-      ptx::tmem_ld_wait();
-    };
-    // Wait for the partner's block of tile t.  With two receive buffers the
-    // warp meanwhile watches for its own scores of tile t + 1 and sends them
-    // the moment they exist (next_sent), so that transfer overlaps the rest
-    // of this wait and the softmax of tile t.
-    auto await_block = [&](int t, bool& next_sent) -> bool {
-      const int rbuf = t % NRECV;
-      const uint32_t rf = ptx::smem_u32(&bars.recv_full[rbuf][sw]);
-      const uint32_t par = (t / NRECV) & 1;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(rf, RECV_W);
-      if (NRECV == 1 || next_sent) return wait_all(c, rf, par);
-      const uint32_t sn = ptx::smem_u32(&bars.s_full[(t + 1) & 1]);
-      const uint32_t sn_par = ((t + 1) >> 1) & 1;
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (true) {
-        if (!next_sent && __all_sync(0xffffffffu, ptx::mbar_test_wait(sn, sn_par))) {
-          uint32_t raw[32];
-          ptx::tc_fence_after();
-          load_scores(t + 1, raw);
-          if (!send_tile(t + 1, raw)) return false;
-          next_sent = true;
-          return wait_all(c, rf, par);
-        }
-        if (__all_sync(0xffffffffu, ptx::mbar_test_wait(rf, par))) return true;
-        if (*c.abort) return false;
-        if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
-          atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
-          *c.abort = 1;
-          return false;
-        }
-        __nanosleep(64);
-      }
-    };
-    // Add the partner's block of tile t (complete) to this warp's partial scores.
-    auto add_block = [&](int t, float (&s)[32]) {
-      const int rbuf = t % NRECV;
-      const uint32_t src = recv_addr(rbuf) + lane * 16;
-      uint32_t fold = 0;
-#pragma unroll
-      for (int qd = 0; qd < 2; ++qd) {
-        uint32_t w[12];
-#pragma unroll
-        for (int v = 0; v < 3; ++v) {
-          const uint4 x = ld_shared_u4(src + (3 * qd + v) * 512);
-          w[4 * v] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
-          fold ^= x.x ^ x.y ^ x.z ^ x.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float u[4];
-          unpack24(w + 3 * k, u);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[16 * qd + 4 * k + e] += u[e];
-        }
-      }
-      // The buffer is read (the vote needs every lane's loaded words): the
-      // partner may send the tile that reuses it.
-      const bool any = __any_sync(0xffffffffu, fold == 0x9E3779B9u);
-      if (t + NRECV < n_tiles && lane == 0)
-        ptx::st_async_b32(ptx::mapa(sbase + L::OFF_XFREE + (rbuf * 8 + sw) * 4, peer),
-                          any ? 1u : 0u,
-                          ptx::mapa(ptx::smem_u32(&bars.recv_free[rbuf][sw]), peer));
-    };
+    const uint32_t my_recv = sbase + OFF_RECV + sw * RECV_W;
+    const uint32_t peer_recv = ptx::mapa(my_recv, peer);
+    const uint32_t peer_free = ptx::mapa(sbase + OFF_RECV + X_FREE + sw * 4, peer);
+    const uint32_t recv_full = ptx::smem_u32(&bars.recv_full[sw]);
+    const uint32_t recv_free = ptx::smem_u32(&bars.recv_free[sw]);
     // A warp whose 16 rows are all past the problem's rows (fewer than 128
     // rows) swaps nothing and computes nothing; it only keeps the barrier
     // phases moving.  Both CTAs skip the same warps.  Its TMEM lanes hold
     // garbage that no output reads (the MMAs keep rows apart).
     const bool live = rb * mla::kRowTile + lbase < p.rows;
     bool ok = true;
-    bool next_sent = false;  // two buffers: tile t + 1 already sent while waiting on tile t
-    for (int t = 0; ok && t < n_tiles; ++t) {
+    for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       if (!wait_all(c, ptx::smem_u32(&bars.s_full[buf]), (t >> 1) & 1)) { ok = false; break; }
       if (!live) {
@@ -759,20 +663,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         continue;
       }
       ptx::tc_fence_after();
+      const uint32_t scol = tmem + lanes16 + TM_S + buf * T;
       float s[32];  // s[4j + e]: e = 0, 1 -> row A keys 8j + 2cq + e; e = 2, 3 -> row B
       {
         uint32_t raw[32];
-        load_scores(t, raw);
+        ptx::tmem_ld16x256b_x8(scol, raw);
+        ptx::tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
-        // this tile's block, unless it went out during the previous wait
-        const bool sent = NRECV == 2 && next_sent;
-        next_sent = false;
-        if (!sent && !send_tile(t, raw)) { ok = false; break; }
       }
-      if (t + 1 >= n_tiles) next_sent = true;  // nothing to send ahead
-      if (!await_block(t, next_sent)) { ok = false; break; }
-      add_block(t, s);
+      // Swap partial-score blocks with the same warp of the partner CTA.  The
+      // block of tile t goes into the partner's (single) buffer once the
+      // partner has read tile t - 1 from it.
+      if (t >= 1) {
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_free, 4);
+        if (!wait_all(c, recv_free, (t - 1) & 1)) { ok = false; break; }
+      }
+      {
+        const uint32_t dst = peer_recv + lane * 16;
+        const uint32_t bar = ptx::mapa(recv_full, peer);
+#pragma unroll
+        for (int qd = 0; qd < 2; ++qd) {  // 16 scores -> 12 words -> 3 stores
+          uint32_t w[12];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // rounded to 24 bits: the top 3 bytes of x + 0x80
+            pack24(round_up_bits(s[16 * qd + 4 * k]), round_up_bits(s[16 * qd + 4 * k + 1]),
+                   round_up_bits(s[16 * qd + 4 * k + 2]), round_up_bits(s[16 * qd + 4 * k + 3]),
+                   w + 3 * k);
+#pragma unroll
+          for (int v = 0; v < 3; ++v)
+            ptx::st_async_u4(dst + (3 * qd + v) * 512, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                             w[4 * v + 3], bar);
+        }
+      }
+      {
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
+        if (!wait_all(c, recv_full, t & 1)) { ok = false; break; }
+        const uint32_t src = my_recv + lane * 16;
+        uint32_t fold = 0;
+#pragma unroll
+        for (int qd = 0; qd < 2; ++qd) {
+          uint32_t w[12];
+#pragma unroll
+          for (int v = 0; v < 3; ++v) {
+            const uint4 x = ld_shared_u4(src + (3 * qd + v) * 512);
+            w[4 * v] = x.x;
+            w[4 * v + 1] = x.y;
+            w[4 * v + 2] = x.z;
+            w[4 * v + 3] = x.w;
+            fold ^= x.x ^ x.y ^ x.z ^ x.w;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float u[4];
+            unpack24(w + 3 * k, u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[16 * qd + 4 * k + e] += u[e];
+          }
+        }
+        // The buffer is read (the vote needs every lane's loaded words): the
+        // partner may send its next tile.
+        const bool any = __any_sync(0xffffffffu, fold == 0x9E3779B9u);
+        if (t + 1 < n_tiles && lane == 0)
+          ptx::st_async_b32(peer_free, any ? 1u : 0u, ptx::mapa(recv_free, peer));
+      }
       // Row maxima over the visible keys of this tile (log2 domain).  Only the
       // last tile of a split and causal rows need the mask.
       const int tile0 = k0 + t * T;
