@@ -94,6 +94,67 @@ def load_peaks():
 
 # ------------------------------------------------------------------- clocks ---
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries) every 0.5 ms while the timed region runs: a region of a few
+    milliseconds still gets several samples.  Raises OSError when NVML is not
+    there; the caller then falls back to nvidia-smi."""
+
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.0005):
+        import ctypes
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = False
+        self.t = None
+        self.max_mhz = self._max_clock()
+
+    def _clock(self):
+        import ctypes
+        v = ctypes.c_uint(0)  # NVML_CLOCK_SM = 1
+        return v.value if self.nv.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(v)) == 0 else None
+
+    def _max_clock(self):
+        import ctypes
+        v = ctypes.c_uint(0)
+        ok = self.nv.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(v)) == 0
+        return v.value if ok else None
+
+    def _reasons(self):
+        import ctypes
+        v = ctypes.c_ulonglong(0)
+        fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return v.value if fn(self.h, ctypes.byref(v)) == 0 else 0
+
+    def _run(self):
+        while not self.stop_flag:
+            self.samples.append((self._clock(), self._reasons()))
+            time.sleep(self.period)
+
+    def start(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        time.sleep(0.01)
+
+    def stop(self):
+        self.stop_flag = True
+        self.t.join(timeout=2)
+        sm = [c for c, _ in self.samples if c]
+        reasons = sorted(n for n, bit in self.REASONS.items()
+                         if any(r & bit for _, r in self.samples))
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "samples": len(sm), "reasons": reasons, "source": "nvml, 0.5 ms"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
 
@@ -341,7 +402,15 @@ def run_gpu(args):
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     ev_f = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    clocks = ClockSampler(dev.index if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
+    gpu_index = dev.index if world == 1 else int(os.environ.get("LOCAL_RANK", 0))
+    try:  # NVML numbers the GPUs of the machine, CUDA the visible ones
+        nvml_index = torch.cuda._get_nvml_device_index(dev)
+    except Exception:
+        nvml_index = gpu_index
+    try:
+        clocks = NvmlClockSampler(nvml_index)
+    except (OSError, AttributeError):
+        clocks = ClockSampler(gpu_index)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
