@@ -70,12 +70,21 @@ constexpr int NR = 3;                   // raw slots (one per loader warp)
 // every accumulator (lanes 32 q + 16 .. 32 q + 31 hold unused rows).  Warp q
 // (0..3) is the softmax warp of quarter q; warps 4-6 load, warp 7 issues the
 // MMAs.  Eight warps leave 255 registers a thread.
+//
+// At most 16 rows (kKS, "key split"): the rows sit in lane quarter 0, which
+// warps 0 and 4 reach, so those two warps share each 128-key tile, 64 keys
+// each, and exchange their row maxima and sums through shared memory; warps
+// 1-3 load, warps 5 and 6 idle.
 constexpr int kLoaders = 3;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 7;
 constexpr int kThreads = 32 * 8;
-__device__ __forceinline__ bool is_softmax_warp(int w) { return w < kSoftmaxWarps; }
-__device__ __forceinline__ int loader_index(int w) { return w - kSoftmaxWarps; }  // warps 4, 5, 6
+template <bool kKS>
+__device__ __forceinline__ bool is_softmax_warp(int w) { return kKS ? (w == 0 || w == 4) : w < 4; }
+template <bool kKS>
+__device__ __forceinline__ bool is_loader_warp(int w) { return kKS ? (w >= 1 && w <= 3) : (w >= 4 && w <= 6); }
+template <bool kKS>
+__device__ __forceinline__ int loader_index(int w) { return kKS ? w - 1 : w - 4; }
 __device__ __forceinline__ int mma_row(int r) { return 32 * (r >> 4) + (r & 15); }
 constexpr int RECV_W = 32 * 16 * 12;    // one warp's partial scores: 16 rows x 128 keys x 3 B (6 KB)
 
@@ -101,7 +110,8 @@ struct Layout {
   static constexpr int OFF_RECV = OFF_RAW + (kFp8 ? NR * RAW_HALF : 0);
   static constexpr int RECV = (max_rows / 16) * RECV_W;
   static constexpr int OFF_XFREE = OFF_RECV + RECV;
-  static constexpr int OFF_BAR = OFF_XFREE + 128;
+  static constexpr int OFF_XMAX = OFF_XFREE + 128;  // key split: [3][2 warps][32 lanes] float4
+  static constexpr int OFF_BAR = OFF_XMAX + 3 * 2 * 32 * 16;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
 };
 static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
@@ -135,6 +145,7 @@ struct Bars {
   uint32_t tmem_base;
   int32_t abort;
   uint64_t heavy[2];
+  uint64_t xchg[3];  // key split: the two softmax warps' maxima (per tile parity) and final sums
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -245,7 +256,7 @@ __device__ __forceinline__ uint64_t vdesc(uint32_t addr) { return ptx::smem_desc
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) * 16); }
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) * 16); }
 
-template <bool kFp8>
+template <bool kFp8, bool kKS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_small_kernel(mla::FwdParams p) {
   using L = Layout<kFp8>;
@@ -313,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * kSoftmaxWarps);
+      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * (kKS ? 2 : kSoftmaxWarps));
     }
     for (int w = 0; w < kSoftmaxWarps; ++w) {
       ptx::mbar_init(ptx::smem_u32(&bars.recv_full[w]), 1);
@@ -321,8 +332,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.o_final), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * kSoftmaxWarps);
+    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * (kKS ? 2 : kSoftmaxWarps));
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
+    for (int i = 0; i < 3; ++i) ptx::mbar_init(ptx::smem_u32(&bars.xchg[i]), 64);
+    bars.heavy[0] = bars.heavy[1] = 0;  // bytes of absent warps stay zero
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
   }
@@ -408,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (!is_softmax_warp(warp)) {
+  } else if (is_loader_warp<kKS>(warp)) {
     // ------------------------------------------------------------ loader ---
     // Loader warp w fills the 64-key halves u = w, w + 3, ... of the split's
     // tile sequence (tile u / 2, keys 64 (u % 2) .. of it) into stage
@@ -423,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         p.bt + (p.bt_indptr ? (size_t)p.bt_indptr[b] : (size_t)b * p.bt_stride);
     const char* cache = static_cast<const char*>(p.cache);
     const int n_halves = 2 * n_tiles;
-    const int lw = loader_index(warp);
+    const int lw = loader_index<kKS>(warp);
     // i-th key of this lane in half u, clamped to the split's last key k1 - 1:
     // a partial half, or the empty second half of a split's last tile,
     // repeats a real row (its weights are masked to zero), so every key read
@@ -538,16 +551,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
     }
     ptx::cp_async_wait<0>();
+  } else if (!is_softmax_warp<kKS>(warp)) {
+    // warps 5 and 6 when the rows fit one lane quarter: no work
   } else {
     // ----------------------------------------------------------- softmax ---
     // As in the 128-row kernel's 16x256b access: warp q owns TMEM lanes
     // 32 q .. 32 q + 15 (problem rows 16 q .. 16 q + 15); thread i holds
     // lanes 32 q + i/4 and + 8 (rows rA = 16 q + i/4, rB = rA + 8) and, of
-    // every 8-key group j of the 128 keys, keys 8j + 2(i%4), 8j + 2(i%4) + 1.
-    // Only warps whose rows are real work; the others keep the barrier
-    // phases moving.
-    const int q4 = warp;
-    const int sw = q4;
+    // every 8-key group j of a 64-key half, keys 8j + 2(i%4), 8j + 2(i%4) + 1.
+    // Without the key split a warp scores both halves of the tile; with it,
+    // warp 4 kh scores half kh.  Only warps whose rows are real work; the
+    // others keep the barrier phases moving.
+    constexpr int NH = kKS ? 1 : 2;          // 64-key halves this warp scores
+    constexpr int NSW = kKS ? 2 : kSoftmaxWarps;
+    const int q4 = warp & 3;
+    const int kh = kKS ? warp >> 2 : 0;      // key half (key split only)
+    const int sw = kKS ? kh : q4;            // index among the softmax warps
     const int lbase = q4 * 32;
     const int cq = lane & 3;
     const int rA = 16 * q4 + (lane >> 2), rB = rA + 8;  // problem rows
@@ -568,7 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     {
       bool q_range = false;
       const int n_pieces = p.rows * 36;  // per row: 4 slabs x 8 chunks + 4 rope chunks
-      for (int i = sw * 32 + lane; i < n_pieces; i += 32 * kSoftmaxWarps) {
+      for (int i = sw * 32 + lane; i < n_pieces; i += 32 * NSW) {
         const int r = i / 36, pc = i % 36, ar = mma_row(r);
         const uint16_t* qrow = p.q + ((size_t)b * p.rows + r) * mla::kDQK;
         uint4 x;
@@ -593,12 +612,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
     float mA = kMaxSentinel, mB = kMaxSentinel;
     float lA = 0.f, lB = 0.f;
-    const int slot = q4;  // receive slot of this warp's rows
-    const uint32_t my_recv = sbase + L::OFF_RECV + slot * RECV_W;
+    // receive slot of this warp's rows: 6 KB a warp, 3 KB a warp under the key split
+    const uint32_t my_recv = sbase + L::OFF_RECV + sw * (RECV_W / 2) * NH;
     const uint32_t peer_recv = ptx::mapa(my_recv, peer);
     const uint32_t peer_free = ptx::mapa(sbase + L::OFF_XFREE + sw * 4, peer);
     const uint32_t recv_full = ptx::smem_u32(&bars.recv_full[sw]);
     const uint32_t recv_free = ptx::smem_u32(&bars.recv_free[sw]);
+    // key split: this warp's and the other warp's slot of the exchange area
+    auto xslot = [&](int i, int w) { return sbase + L::OFF_XMAX + (i * 2 + w) * 512 + lane * 16; };
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
@@ -610,19 +631,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t scol = tmem + lanes16 + TM_S + buf * T;
-      // s[32 hf + 4 j + e]: key half hf (keys 64 hf ..), 8-key group j;
-      // e = 0, 1 -> row A keys 8j + 2cq + e; e = 2, 3 -> row B
-      float s[64];
+      // s[32 hh + 4 j + e]: the warp's key half hh (key half kh under the
+      // key split), 8-key group j; e = 0, 1 -> row A keys 8j + 2cq + e;
+      // e = 2, 3 -> row B
+      float s[32 * NH];
       {
-        uint32_t raw[2][32];
-        ptx::tmem_ld16x256b_x8(scol, raw[0]);
-        ptx::tmem_ld16x256b_x8(scol + 64, raw[1]);
+        uint32_t raw[NH][32];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) ptx::tmem_ld16x256b_x8(scol + (kKS ? kh : hh) * 64, raw[hh]);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(raw[0][i]);
-          s[32 + i] = __uint_as_float(raw[1][i]);
-        }
+        for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * hh + i] = __uint_as_float(raw[hh][i]);
       }
       // Swap partial scores with the same warp of the partner CTA (single
       // receive buffer: tile t goes once the partner has read tile t - 1).
@@ -634,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t dst = peer_recv + lane * 16;
         const uint32_t bar = ptx::mapa(recv_full, peer);
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {  // 16 scores -> 12 words -> 3 stores
+        for (int qd = 0; qd < 2 * NH; ++qd) {  // 16 scores -> 12 words -> 3 stores
           uint32_t w[12];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -648,12 +669,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       {
-        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, NH * (RECV_W / 2));
         if (!wait_all(c, recv_full, t & 1)) { ok = false; break; }
         const uint32_t src = my_recv + lane * 16;
         uint32_t fold = 0;
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
+        for (int qd = 0; qd < 2 * NH; ++qd) {
           uint32_t w[12];
 #pragma unroll
           for (int v = 0; v < 3; ++v) {
@@ -682,16 +703,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float mxA = -INFINITY, mxB = -INFINITY;
       if (all_full) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8 * NH; ++j) {
           mxA = fmaxf(mxA, fmaxf(s[4 * j], s[4 * j + 1]));
           mxB = fmaxf(mxB, fmaxf(s[4 * j + 2], s[4 * j + 3]));
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < 8 * NH; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int k = 8 * j + 2 * cq + e;
+            const int k = 64 * kh + 8 * j + 2 * cq + e;
             if (k < limA) mxA = fmaxf(mxA, s[4 * j + e]);
             if (k < limB) mxB = fmaxf(mxB, s[4 * j + 2 + e]);
           }
@@ -700,12 +721,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
       mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+      // Key split: the two warps of the quarter trade their half-tile maxima
+      // and their sums so far (the same lane holds the same rows in both),
+      // so that both take the same rescale decisions and keep one running
+      // max.  Two slots by tile parity: a warp writes slot t % 2 again only
+      // after the other has passed tile t + 1's exchange, so after it read
+      // tile t's values.
+      float olA = 0.f, olB = 0.f;
+      if constexpr (kKS) {
+        st_shared_u4(xslot(buf, kh), make_uint4(__float_as_uint(mxA), __float_as_uint(mxB),
+                                                __float_as_uint(lA), __float_as_uint(lB)));
+        ptx::mbar_arrive(ptx::smem_u32(&bars.xchg[buf]));
+        if (!wait_all(c, ptx::smem_u32(&bars.xchg[buf]), (t >> 1) & 1)) { ok = false; break; }
+        const uint4 o = ld_shared_u4(xslot(buf, kh ^ 1));
+        mxA = fmaxf(mxA, __uint_as_float(o.x));
+        mxB = fmaxf(mxB, __uint_as_float(o.y));
+        olA = __uint_as_float(o.z);
+        olB = __uint_as_float(o.w);
+      }
       const float mtA = limA > 0 ? mxA * c2 : -INFINITY;
       const float mtB = limB > 0 ? mxB * c2 : -INFINITY;
       const bool needA = mtA > mA + kRescaleThreshold, needB = mtB > mB + kRescaleThreshold;
+      float alA = 1.f, alB = 1.f;
       if (__any_sync(0xffffffffu, needA || needB)) {
         const float nA = needA ? fmaxf(mA, mtA) : mA, nB = needB ? fmaxf(mB, mtB) : mB;
-        const float alA = exp2f(mA - nA), alB = exp2f(mB - nB);
+        alA = exp2f(mA - nA);
+        alB = exp2f(mB - nB);
         if (t > 0) {
           // The PV of the previous tile must have finished: QK^T of this
           // tile was issued after PV of tile t - 2 and the pipe runs in
@@ -713,7 +754,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!wait_all(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
+          for (int ch = 2 * kh; ch < (kKS ? 2 * kh + 2 : 4); ++ch) {
             uint32_t o[32];
             const uint32_t col = tmem + lanes16 + TM_O + ch * 64;
             ptx::tmem_ld16x256b_x8(col, o);
@@ -735,11 +776,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float sA = 0.f, sB = 0.f;
       const uint32_t pcol = tmem + lanes16 + TM_S + buf * T;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int hh = 0; hh < NH; ++hh) {
+        const int hf = kKS ? kh : hh;  // the key half in the tile
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int j8 = 0; j8 < 8; ++j8) {
-          const int j = 8 * hf + j8, k = 8 * j + 2 * cq;
+          const int j = 8 * hh + j8, k = 64 * hf + 8 * j8 + 2 * cq;
           float a0 = fast_exp2(fmaf(s[4 * j], c2, nmA));
           float a1 = fast_exp2(fmaf(s[4 * j + 1], c2, nmA));
           float b0 = fast_exp2(fmaf(s[4 * j + 2], c2, nmB));
@@ -768,11 +810,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       lB += sB;
       if constexpr (!kFp8) {
         // The low-order terms are written for every tile; the second PV runs
-        // only where one key carries more than 1/16 of a row's weight.
+        // only where one key carries more than 1/16 of a row's weight.  Under
+        // the key split the row's sum counts the other warp's keys up to the
+        // previous tile only, which errs towards the second PV.
         const float pmA = limA > 0 ? fast_exp2(mtA - mA) : 0.f;
         const float pmB = limB > 0 ? fast_exp2(mtB - mB) : 0.f;
-        float rsA = lA + __shfl_xor_sync(0xffffffffu, lA, 1);
-        float rsB = lB + __shfl_xor_sync(0xffffffffu, lB, 1);
+        float rsA = lA + olA * alA, rsB = lB + olB * alB;
+        rsA += __shfl_xor_sync(0xffffffffu, rsA, 1);
+        rsB += __shfl_xor_sync(0xffffffffu, rsB, 1);
         rsA += __shfl_xor_sync(0xffffffffu, rsA, 2);
         rsB += __shfl_xor_sync(0xffffffffu, rsB, 2);
         const bool heavy = __any_sync(0xffffffffu, pmA * 16.f > rsA || pmB * 16.f > rsB);
@@ -784,6 +829,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue ---
+    if constexpr (kKS) {
+      // the other warp's share of the row sums
+      if (ok) {
+        st_shared_u4(xslot(2, kh), make_uint4(__float_as_uint(lA), __float_as_uint(lB), 0u, 0u));
+        ptx::mbar_arrive(ptx::smem_u32(&bars.xchg[2]));
+        if (wait_all(c, ptx::smem_u32(&bars.xchg[2]), 0)) {
+          const uint4 o = ld_shared_u4(xslot(2, kh ^ 1));
+          lA += __uint_as_float(o.x);
+          lB += __uint_as_float(o.y);
+        } else {
+          ok = false;
+        }
+      }
+    }
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -795,7 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const size_t pA = part * p.rows + rA;  // problem rows (TMEM lanes are spread)
       const size_t pB = part * p.rows + rB;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * kh; ch < (kKS ? 2 * kh + 2 : 4); ++ch) {
         uint32_t o[32];
         ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_O + ch * 64, o);
         ptx::tmem_ld_wait();
@@ -813,7 +872,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (rank == 0 && cq == 0) {
+      if (rank == 0 && cq == 0 && kh == 0) {
         const float lseA = lA > 0.f ? (mA + log2f(lA)) * 0.6931471805599453f : -INFINITY;
         const float lseB = lB > 0.f ? (mB + log2f(lB)) * 0.6931471805599453f : -INFINITY;
         if (single) {
@@ -852,12 +911,14 @@ bool mla_small_rows_fit(int rows, int kv_dtype) {
 
 int mla_launch_fwd_small_sm103(const mla::FwdParams& p, void* stream) {
   const bool fp8 = p.kv_dtype == MLA_KV_FP8_E4M3;
-  auto kernel = fp8 ? fwd_small_kernel<true> : fwd_small_kernel<false>;
+  const bool ks = p.rows <= 16;  // the rows fit one TMEM lane quarter: split the keys
+  auto kernel = fp8 ? (ks ? fwd_small_kernel<true, true> : fwd_small_kernel<true, false>)
+                    : (ks ? fwd_small_kernel<false, true> : fwd_small_kernel<false, false>);
   const int smem = fp8 ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, fp8 ? 4 : 3);
+  e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, (fp8 ? 4 : 3) + (ks ? 2 : 0));
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.units != nullptr ? dim3(2 * p.unit_capacity, 1, 1)
