@@ -28,11 +28,13 @@
 // softmax in the softmax warps whose 16-row block holds real rows.
 //
 // Per 128-key tile:
-//   loader warps  : three warps, each owning 64-key halves 3i + w of the
-//                   tile sequence: block-table lookup, 16-byte cp.async of
-//                   the half's row pieces into the tile's stage (bf16) or
-//                   into the warp's raw slot, converted to f16 by the same
-//                   lanes (fp8); both halves arrive on the stage's barrier.
+//   loader warps  : three warps, each owning parts 3i + w of the tile
+//                   sequence (64 keys for bf16, 32 for fp8): block-table
+//                   lookup, 16-byte cp.async of the part's row pieces into
+//                   the tile's stage (bf16) or into one of the warp's two raw
+//                   slots, converted to f16 by the same lanes (fp8, the next
+//                   part's copy already in flight); every part arrives on the
+//                   stage's barrier.
 //   MMA warp      : S_part = Q_part K_part^T (18 MMAs, N = 128, A = Q from
 //                   shared memory), then O_half += P V_half (8 MMAs, N =
 //                   256, A = P from TMEM, B = the same stage read MN-major;
@@ -56,13 +58,16 @@
 namespace {
 
 constexpr int T = mla::kKeyTileSmall;   // 128 keys per tile
-constexpr int HALF = T / 2;             // keys a loader warp fills at a time
 constexpr int ATOM = T * 128;           // one 64-dim latent slab of a stage: 16 KB
 constexpr int RATOM = T * 64;           // the CTA's rope half, 64-byte rows: 8 KB
 constexpr int STAGE = 4 * ATOM + RATOM; // 72 KB
 constexpr int NS = 2;                   // operand stages (one tile each)
-constexpr int RAW_HALF = HALF * (256 + 32);  // fp8 codes of a half: 18 KB
-constexpr int NR = 3;                   // raw slots (one per loader warp)
+template <bool kFp8>
+struct LoadPart {
+  static constexpr int keys = kFp8 ? 32 : 64;  // keys of one loader part
+};
+constexpr int RAW_PART = 32 * (256 + 32);      // fp8 codes of a 32-key part: 9 KB
+constexpr int NR = 6;                          // raw slots (two per loader warp)
 // Rows and warps: a warp reaches only the TMEM lane quarter warp % 4, and
 // each quarter belongs to one SM sub-partition.  So that all four
 // sub-partitions share the softmax, the (at most 64) rows are spread 16 to a
@@ -107,7 +112,7 @@ struct Layout {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_STAGE = (qbytes() + 1023) / 1024 * 1024;  // 40 KB bf16, 9 KB fp8
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
-  static constexpr int OFF_RECV = OFF_RAW + (kFp8 ? NR * RAW_HALF : 0);
+  static constexpr int OFF_RECV = OFF_RAW + (kFp8 ? NR * RAW_PART : 0);
   static constexpr int RECV = (max_rows / 16) * RECV_W;
   static constexpr int OFF_XFREE = OFF_RECV + RECV;
   static constexpr int OFF_XMAX = OFF_XFREE + 128;  // key split: [3][2 warps][32 lanes] float4
@@ -132,7 +137,7 @@ constexpr uint64_t kDrainNs = 500000000ull;
 constexpr uint32_t kSleepNs = 20000;
 
 struct Bars {
-  uint64_t kv_full[NS];   // both halves of the stage landed (2 x 32 loader lanes)
+  uint64_t kv_full[NS];   // every loader part of the stage landed (32 lanes a part)
   uint64_t kv_empty[NS];  // the stage's MMAs are done
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -261,6 +266,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_small_kernel(mla::FwdParams p) {
   using L = Layout<kFp8>;
   constexpr uint32_t kAB = kFp8 ? 0u : 1u;
+  constexpr int PART = LoadPart<kFp8>::keys;
+  constexpr int UPT = T / PART;  // loader parts per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -319,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 64);
+      ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 32 * UPT);
       ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -423,26 +430,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (is_loader_warp<kKS>(warp)) {
     // ------------------------------------------------------------ loader ---
-    // Loader warp w fills the 64-key halves u = w, w + 3, ... of the split's
-    // tile sequence (tile u / 2, keys 64 (u % 2) .. of it) into stage
-    // (u / 2) % 2.  A key's piece of a 64-dim latent slab is 128 bytes (8
-    // lanes x 16 B for bf16, 4 lanes x 16 codes for fp8) and its rope half 64
-    // bytes (4 lanes of bf16, 2 of fp8).
+    // The tile sequence of the split is cut into parts of PART keys (64 for
+    // bf16, 32 for fp8); loader warp w fills parts u = w, w + 3, ... (tile
+    // u / UPT, keys PART (u % UPT) .. of it) into stage (u / UPT) % 2.  A key's
+    // piece of a 64-dim latent slab is 128 bytes (8 lanes x 16 B for bf16, 4
+    // lanes x 16 codes for fp8) and its rope half 64 bytes (4 lanes of bf16,
+    // 2 of fp8).  bf16 copies go straight into the stage once it is free.
+    // fp8 codes go into one of the warp's two raw slots and are converted to
+    // f16 by the same lanes; the copy of the warp's next part is issued before
+    // the current one waits for its stage and converts, so a part is always in
+    // flight.
     constexpr int LPI = kFp8 ? 4 : 8;  // lanes per 128-byte latent piece
     constexpr int IPI = 32 / LPI;      // keys per warp instruction
-    constexpr int NK = HALF / IPI;     // keys per lane and half: 8 (bf16) or 4 (fp8)
+    constexpr int NK = PART / IPI;     // keys per lane and part: 16 (bf16) or 4 (fp8)
     const int g = lane / LPI, sub = lane % LPI;
     const int32_t* bt =
         p.bt + (p.bt_indptr ? (size_t)p.bt_indptr[b] : (size_t)b * p.bt_stride);
     const char* cache = static_cast<const char*>(p.cache);
-    const int n_halves = 2 * n_tiles;
+    const int n_units = UPT * n_tiles;
     const int lw = loader_index<kKS>(warp);
-    // i-th key of this lane in half u, clamped to the split's last key k1 - 1:
-    // a partial half, or the empty second half of a split's last tile,
-    // repeats a real row (its weights are masked to zero), so every key read
-    // lies in [k0, k1) and no stage slot the value MMA reads holds anything
-    // but cache rows.
-    auto key_of = [&](int u, int i) -> int { return min(k0 + u * HALF + i * IPI + g, k1 - 1); };
+    // i-th key of this lane in part u, clamped to the split's last key k1 - 1:
+    // a partial part, or the empty parts of a split's last tile, repeat a real
+    // row (its weights are masked to zero), so every key read lies in
+    // [k0, k1) and no stage slot the value MMA reads holds anything but cache
+    // rows.
+    auto key_of = [&](int u, int i) -> int { return min(k0 + u * PART + i * IPI + g, k1 - 1); };
     const uint32_t pdiv = (uint32_t)p.page_size;
     const uint32_t plog = 32u - __clz(pdiv - 1u);
     const uint32_t pmul = (uint32_t)(((1ull << 32) * ((1ull << plog) - pdiv)) / pdiv) + 1u;
@@ -453,14 +465,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     int pg[NK];
     auto load_pages = [&](int u) {
-      if (u >= n_halves) return;
+      if (u >= n_units) return;
 #pragma unroll
       for (int i = 0; i < NK; ++i) pg[i] = __ldg(&bt[page_of((uint32_t)key_of(u, i))]);
     };
-    load_pages(lw);
-    for (int u = lw; u < n_halves; u += kLoaders) {
-      const int t = u >> 1, h = u & 1, s = t % NS;
-      uint32_t rix[NK];  // cache row of each key (num_pages * page_size < 2^31)
+    uint32_t rix[NK];  // cache row of each key of a part (num_pages * page_size < 2^31)
+    auto rows_of = [&](int u) {  // from the block-table entries in pg
       bool bad = false;
 #pragma unroll
       for (int i = 0; i < NK; ++i) {
@@ -472,83 +482,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t key = (uint32_t)key_of(u, i);
         rix[i] = (uint32_t)page * pdiv + (key - page_of(key) * pdiv);
       }
-      auto row = [&](int i) { return cache + (size_t)rix[i] * (kFp8 ? mla::kDQK : mla::kDQK * 2); };
       if (bad) atomicOr(p.status, MLA_DEVFLAG_BAD_PAGE);
-      load_pages(u + kLoaders);
-      const uint32_t stage = sbase + L::OFF_STAGE + s * STAGE;
-      if constexpr (!kFp8) {
+    };
+    auto row = [&](int i) { return cache + (size_t)rix[i] * (kFp8 ? mla::kDQK : mla::kDQK * 2); };
+    load_pages(lw);
+    if constexpr (!kFp8) {
+      for (int u = lw; u < n_units; u += kLoaders) {
+        const int t = u / UPT, h = u % UPT, s = t % NS;
+        rows_of(u);
+        load_pages(u + kLoaders);
+        const uint32_t stage = sbase + L::OFF_STAGE + s * STAGE;
         if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) break;
-        {
 #pragma unroll
-          for (int i = 0; i < NK; ++i) {
-            const int kk = h * HALF + i * IPI + g;  // key within the tile
+        for (int i = 0; i < NK; ++i) {
+          const int kk = h * PART + i * IPI + g;  // key within the tile
 #pragma unroll
-            for (int sl = 0; sl < 4; ++sl)
-              ptx::cp_async_16(stage + sl * ATOM + sw128(kk, sub),
-                               row(i) + (vdim0 + sl * 64 + sub * 8) * 2);
-            if (sub < 4)  // the CTA's rope half: dims 512 + 32 rank + 8 sub
-              ptx::cp_async_16(stage + 4 * ATOM + sw64(kk, sub),
-                               row(i) + (512 + 32 * (int)rank + sub * 8) * 2);
-          }
+          for (int sl = 0; sl < 4; ++sl)
+            ptx::cp_async_16(stage + sl * ATOM + sw128(kk, sub), row(i) + (vdim0 + sl * 64 + sub * 8) * 2);
+          if (sub < 4)  // the CTA's rope half: dims 512 + 32 rank + 8 sub
+            ptx::cp_async_16(stage + 4 * ATOM + sw64(kk, sub), row(i) + (512 + 32 * (int)rank + sub * 8) * 2);
         }
         ptx::cp_async_commit();
         ptx::cp_async_wait<0>();
-      } else {
-        const uint32_t raw = sbase + L::OFF_RAW + lw * RAW_HALF;  // [64 keys][288 codes]
-        {
-#pragma unroll
-          for (int i = 0; i < NK; ++i) {
-            const int kr = i * IPI + g;  // key within the half
-#pragma unroll
-            for (int sl = 0; sl < 4; ++sl)
-              ptx::cp_async_16(raw + kr * 288 + sl * 64 + sub * 16, row(i) + vdim0 + sl * 64 + sub * 16);
-            if (sub < 2)
-              ptx::cp_async_16(raw + kr * 288 + 256 + sub * 16, row(i) + 512 + 32 * (int)rank + sub * 16);
-          }
-        }
-        ptx::cp_async_commit();
-        ptx::cp_async_wait<0>();
-        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) break;
-        {
-          // e4m3 codes -> f16 operands (exact); the per-tensor scale goes to
-          // the scores and the output instead
-#pragma unroll
-          for (int i = 0; i < NK; ++i) {
-            const int kr = i * IPI + g, kk = h * HALF + kr;
-#pragma unroll
-            for (int sl = 0; sl < 4; ++sl) {
-              const uint4 x = ld_shared_u4(raw + kr * 288 + sl * 64 + sub * 16);
-              uint4 lo, hi;
-              lo.x = e4m3x2_to_f16x2(x.x);
-              lo.y = e4m3x2_to_f16x2(x.x >> 16);
-              lo.z = e4m3x2_to_f16x2(x.y);
-              lo.w = e4m3x2_to_f16x2(x.y >> 16);
-              hi.x = e4m3x2_to_f16x2(x.z);
-              hi.y = e4m3x2_to_f16x2(x.z >> 16);
-              hi.z = e4m3x2_to_f16x2(x.w);
-              hi.w = e4m3x2_to_f16x2(x.w >> 16);
-              st_shared_u4(stage + sl * ATOM + sw128(kk, 2 * sub), lo);
-              st_shared_u4(stage + sl * ATOM + sw128(kk, 2 * sub + 1), hi);
-            }
-            if (sub < 2) {
-              const uint4 x = ld_shared_u4(raw + kr * 288 + 256 + sub * 16);
-              uint4 lo, hi;
-              lo.x = e4m3x2_to_f16x2(x.x);
-              lo.y = e4m3x2_to_f16x2(x.x >> 16);
-              lo.z = e4m3x2_to_f16x2(x.y);
-              lo.w = e4m3x2_to_f16x2(x.y >> 16);
-              hi.x = e4m3x2_to_f16x2(x.z);
-              hi.y = e4m3x2_to_f16x2(x.z >> 16);
-              hi.z = e4m3x2_to_f16x2(x.w);
-              hi.w = e4m3x2_to_f16x2(x.w >> 16);
-              st_shared_u4(stage + 4 * ATOM + sw64(kk, 2 * sub), lo);
-              st_shared_u4(stage + 4 * ATOM + sw64(kk, 2 * sub + 1), hi);
-            }
-          }
-        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
+    } else {
+      // raw slot j of this warp: [PART keys][288 codes]
+      auto raw_slot = [&](int j) { return sbase + L::OFF_RAW + (2 * lw + j) * RAW_PART; };
+      auto issue_raw = [&](int u, int j) {
+        rows_of(u);
+        const uint32_t raw = raw_slot(j);
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const int kr = i * IPI + g;  // key within the part
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl)
+            ptx::cp_async_16(raw + kr * 288 + sl * 64 + sub * 16, row(i) + vdim0 + sl * 64 + sub * 16);
+          if (sub < 2)
+            ptx::cp_async_16(raw + kr * 288 + 256 + sub * 16, row(i) + 512 + 32 * (int)rank + sub * 16);
+        }
+      };
+      if (lw < n_units) issue_raw(lw, 0);
+      ptx::cp_async_commit();
+      load_pages(lw + kLoaders);
+      int j = 0;
+      for (int u = lw; u < n_units; u += kLoaders, j ^= 1) {
+        const int un = u + kLoaders;
+        if (un < n_units) {
+          issue_raw(un, j ^ 1);
+          load_pages(un + kLoaders);
+        }
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<1>();  // this lane's copies of part u have landed
+        const int t = u / UPT, h = u % UPT, s = t % NS;
+        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) break;
+        // e4m3 codes -> f16 operands (exact); the per-tensor scale goes to
+        // the scores and the output instead.  A lane converts the codes it
+        // copied.
+        const uint32_t stage = sbase + L::OFF_STAGE + s * STAGE;
+        const uint32_t raw = raw_slot(j);
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const int kr = i * IPI + g, kk = h * PART + kr;
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) {
+            const uint4 x = ld_shared_u4(raw + kr * 288 + sl * 64 + sub * 16);
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_f16x2(x.x);
+            lo.y = e4m3x2_to_f16x2(x.x >> 16);
+            lo.z = e4m3x2_to_f16x2(x.y);
+            lo.w = e4m3x2_to_f16x2(x.y >> 16);
+            hi.x = e4m3x2_to_f16x2(x.z);
+            hi.y = e4m3x2_to_f16x2(x.z >> 16);
+            hi.z = e4m3x2_to_f16x2(x.w);
+            hi.w = e4m3x2_to_f16x2(x.w >> 16);
+            st_shared_u4(stage + sl * ATOM + sw128(kk, 2 * sub), lo);
+            st_shared_u4(stage + sl * ATOM + sw128(kk, 2 * sub + 1), hi);
+          }
+          if (sub < 2) {
+            const uint4 x = ld_shared_u4(raw + kr * 288 + 256 + sub * 16);
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_f16x2(x.x);
+            lo.y = e4m3x2_to_f16x2(x.x >> 16);
+            lo.z = e4m3x2_to_f16x2(x.y);
+            lo.w = e4m3x2_to_f16x2(x.y >> 16);
+            hi.x = e4m3x2_to_f16x2(x.z);
+            hi.y = e4m3x2_to_f16x2(x.z >> 16);
+            hi.z = e4m3x2_to_f16x2(x.w);
+            hi.w = e4m3x2_to_f16x2(x.w >> 16);
+            st_shared_u4(stage + 4 * ATOM + sw64(kk, 2 * sub), lo);
+            st_shared_u4(stage + 4 * ATOM + sw64(kk, 2 * sub + 1), hi);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
+      }
     }
     ptx::cp_async_wait<0>();
   } else if (!is_softmax_warp<kKS>(warp)) {
