@@ -39,8 +39,10 @@
 //                   shared memory), then O_half += P V_half (8 MMAs, N =
 //                   256, A = P from TMEM, B = the same stage read MN-major;
 //                   8 more with the low-order weights on heavy tiles).
-//   softmax warps : as in the 128-row kernel, over 128 keys: 64 scores a
-//                   thread, 6 KB swapped per warp and tile.
+//   softmax warps : as in the 128-row kernel, two warps per 16-row quarter,
+//                   each over one 64-key half of the tile: 32 scores a
+//                   thread, 3 KB swapped per warp and tile, row maxima and
+//                   sums traded with the other warp of the quarter.
 //
 // Every wait is bounded (2 s unless the plan sets another limit); a wait
 // that runs out sets MLA_DEVFLAG_TIMEOUT and the CTA winds down.
@@ -72,26 +74,31 @@ constexpr int NR = 6;                          // raw slots (two per loader warp
 // each quarter belongs to one SM sub-partition.  So that all four
 // sub-partitions share the softmax, the (at most 64) rows are spread 16 to a
 // quarter: row 16 q + i of the problem is row 32 q + i of the MMA's A and of
-// every accumulator (lanes 32 q + 16 .. 32 q + 31 hold unused rows).  Warp q
-// (0..3) is the softmax warp of quarter q; warps 4-6 load, warp 7 issues the
-// MMAs.  Eight warps leave 255 registers a thread.
+// every accumulator (lanes 32 q + 16 .. 32 q + 31 hold unused rows).
 //
-// At most 16 rows (kKS, "key split"): the rows sit in lane quarter 0, which
-// warps 0 and 4 reach, so those two warps share each 128-key tile, 64 keys
-// each, and exchange their row maxima and sums through shared memory; warps
-// 1-3 load, warps 5 and 6 idle.
+// Key split: the two warps that reach a quarter (q and q + 4) share each
+// 128-key tile, 64 keys each (key half kh = warp / 4), and trade their row
+// maxima and sums through shared memory, so a softmax warp holds 32 scores a
+// thread.  Two forms:
+//   narrow (at most 16 rows, quarter 0 only): 8 warps; 0 and 4 softmax,
+//     1-3 load, 5 and 6 idle, 7 issues the MMAs;
+//   wide (17 to 64 rows, bf16): 12 warps; 0-7 softmax (two per quarter),
+//     8-10 load, 11 issues the MMAs (168 registers a thread).
 constexpr int kLoaders = 3;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kMmaWarp = 7;
-constexpr int kThreads = 32 * 8;
-template <bool kKS>
-__device__ __forceinline__ bool is_softmax_warp(int w) { return kKS ? (w == 0 || w == 4) : w < 4; }
-template <bool kKS>
-__device__ __forceinline__ bool is_loader_warp(int w) { return kKS ? (w >= 1 && w <= 3) : (w >= 4 && w <= 6); }
-template <bool kKS>
-__device__ __forceinline__ int loader_index(int w) { return kKS ? w - 1 : w - 4; }
+template <bool kWide>
+struct Warps {
+  static constexpr int count = kWide ? 12 : 8;
+  static constexpr int softmax = kWide ? 8 : 2;
+  static constexpr int mma = kWide ? 11 : 7;
+};
+template <bool kWide>
+__device__ __forceinline__ bool is_softmax_warp(int w) { return kWide ? w < 8 : (w == 0 || w == 4); }
+template <bool kWide>
+__device__ __forceinline__ bool is_loader_warp(int w) { return kWide ? (w >= 8 && w <= 10) : (w >= 1 && w <= 3); }
+template <bool kWide>
+__device__ __forceinline__ int loader_index(int w) { return kWide ? w - 8 : w - 1; }
 __device__ __forceinline__ int mma_row(int r) { return 32 * (r >> 4) + (r & 15); }
-constexpr int RECV_W = 32 * 16 * 12;    // one warp's partial scores: 16 rows x 128 keys x 3 B (6 KB)
+constexpr int RECV_W = 32 * 16 * 6;     // one warp's partial scores: 16 rows x 64 keys x 3 B (3 KB)
 
 template <bool kFp8>
 struct Layout {
@@ -113,10 +120,11 @@ struct Layout {
   static constexpr int OFF_STAGE = (qbytes() + 1023) / 1024 * 1024;  // 40 KB bf16, 9 KB fp8
   static constexpr int OFF_RAW = OFF_STAGE + NS * STAGE;
   static constexpr int OFF_RECV = OFF_RAW + (kFp8 ? NR * RAW_PART : 0);
-  static constexpr int RECV = (max_rows / 16) * RECV_W;
+  static constexpr int RECV = (max_rows / 16) * 2 * RECV_W;  // two softmax warps a quarter
   static constexpr int OFF_XFREE = OFF_RECV + RECV;
-  static constexpr int OFF_XMAX = OFF_XFREE + 128;  // key split: [3][2 warps][32 lanes] float4
-  static constexpr int OFF_BAR = OFF_XMAX + 3 * 2 * 32 * 16;
+  // the key-split exchange: [quarter][3 slots][2 warps][32 lanes] x 16 B
+  static constexpr int OFF_XMAX = OFF_XFREE + 128;
+  static constexpr int OFF_BAR = OFF_XMAX + (max_rows / 16) * 3 * 2 * 32 * 16;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
 };
 static_assert(Layout<false>::SMEM_BYTES <= 232448, "bf16 smem");
@@ -141,8 +149,8 @@ struct Bars {
   uint64_t kv_empty[NS];  // the stage's MMAs are done
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t recv_full[kSoftmaxWarps];
-  uint64_t recv_free[kSoftmaxWarps];
+  uint64_t recv_full[8];  // per softmax warp
+  uint64_t recv_free[8];
   uint64_t o_done;
   uint64_t o_final;
   uint64_t q_ready;
@@ -150,7 +158,7 @@ struct Bars {
   uint32_t tmem_base;
   int32_t abort;
   uint64_t heavy[2];
-  uint64_t xchg[3];  // key split: the two softmax warps' maxima (per tile parity) and final sums
+  uint64_t xchg[4][3];  // per quarter: the two warps' maxima (per tile parity) and final sums
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -261,8 +269,8 @@ __device__ __forceinline__ uint64_t vdesc(uint32_t addr) { return ptx::smem_desc
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) * 16); }
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) * 16); }
 
-template <bool kFp8, bool kKS>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kFp8, bool kWide>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count * 32, 1)
     fwd_small_kernel(mla::FwdParams p) {
   using L = Layout<kFp8>;
   constexpr uint32_t kAB = kFp8 ? 0u : 1u;
@@ -312,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (n_tiles == 0) {
     ptx::grid_dependency_wait();
-    for (int row = threadIdx.x; row < p.rows; row += kThreads) {
+    for (int row = threadIdx.x; row < p.rows; row += blockDim.x) {
       if (single) {
         uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.rows + row) * mla::kDV + vdim0);
         for (int c = 0; c < 32; ++c) o[c] = make_uint4(0, 0, 0, 0);
@@ -331,22 +339,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * (kKS ? 2 : kSoftmaxWarps));
+      ptx::mbar_init(ptx::smem_u32(&bars.p_full[i]), 32 * Warps<kWide>::softmax);
     }
-    for (int w = 0; w < kSoftmaxWarps; ++w) {
+    for (int w = 0; w < 8; ++w) {
       ptx::mbar_init(ptx::smem_u32(&bars.recv_full[w]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.recv_free[w]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars.o_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars.o_final), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * (kKS ? 2 : kSoftmaxWarps));
+    ptx::mbar_init(ptx::smem_u32(&bars.q_ready), 32 * Warps<kWide>::softmax);
     ptx::mbar_init(ptx::smem_u32(&bars.drain), 1);
-    for (int i = 0; i < 3; ++i) ptx::mbar_init(ptx::smem_u32(&bars.xchg[i]), 64);
+    for (int q = 0; q < 4; ++q)
+      for (int i = 0; i < 3; ++i) ptx::mbar_init(ptx::smem_u32(&bars.xchg[q][i]), 64);
     bars.heavy[0] = bars.heavy[1] = 0;  // bytes of absent warps stay zero
     bars.abort = 0;
     ptx::fence_mbar_init_cluster();
   }
-  if (warp == kMmaWarp) {
+  if (warp == Warps<kWide>::mma) {
     ptx::tmem_alloc(ptx::smem_u32(&bars.tmem_base), TM_COLS);
     ptx::tmem_relinquish();
   }
@@ -357,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort, p.wait_ns};
 
-  if (warp == kMmaWarp) {
+  if (warp == Warps<kWide>::mma) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
       const uint32_t id_qk = ptx::idesc_f16(128, T, kAB, false, false);
@@ -428,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)ok;
     }
     __syncwarp();
-  } else if (is_loader_warp<kKS>(warp)) {
+  } else if (is_loader_warp<kWide>(warp)) {
     // ------------------------------------------------------------ loader ---
     // The tile sequence of the split is cut into parts of PART keys (64 for
     // bf16, 32 for fp8); loader warp w fills parts u = w, w + 3, ... (tile
@@ -448,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         p.bt + (p.bt_indptr ? (size_t)p.bt_indptr[b] : (size_t)b * p.bt_stride);
     const char* cache = static_cast<const char*>(p.cache);
     const int n_units = UPT * n_tiles;
-    const int lw = loader_index<kKS>(warp);
+    const int lw = loader_index<kWide>(warp);
     // i-th key of this lane in part u, clamped to the split's last key k1 - 1:
     // a partial part, or the empty parts of a split's last tile, repeat a real
     // row (its weights are masked to zero), so every key read lies in
@@ -580,22 +589,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     ptx::cp_async_wait<0>();
-  } else if (!is_softmax_warp<kKS>(warp)) {
-    // warps 5 and 6 when the rows fit one lane quarter: no work
+  } else if (!is_softmax_warp<kWide>(warp)) {
+    // warps 5 and 6 of the narrow form: no work
   } else {
     // ----------------------------------------------------------- softmax ---
     // As in the 128-row kernel's 16x256b access: warp q owns TMEM lanes
     // 32 q .. 32 q + 15 (problem rows 16 q .. 16 q + 15); thread i holds
     // lanes 32 q + i/4 and + 8 (rows rA = 16 q + i/4, rB = rA + 8) and, of
-    // every 8-key group j of a 64-key half, keys 8j + 2(i%4), 8j + 2(i%4) + 1.
-    // Without the key split a warp scores both halves of the tile; with it,
-    // warp 4 kh scores half kh.  Only warps whose rows are real work; the
-    // others keep the barrier phases moving.
-    constexpr int NH = kKS ? 1 : 2;          // 64-key halves this warp scores
-    constexpr int NSW = kKS ? 2 : kSoftmaxWarps;
+    // every 8-key group j of its 64-key half kh, keys 64 kh + 8j + 2(i%4) and
+    // + 1.  Only warps whose rows are real work; the others keep the barrier
+    // phases moving.
+    constexpr int NSW = Warps<kWide>::softmax;
     const int q4 = warp & 3;
-    const int kh = kKS ? warp >> 2 : 0;      // key half (key split only)
-    const int sw = kKS ? kh : q4;            // index among the softmax warps
+    const int kh = warp >> 2;     // key half
+    const int sw = 2 * q4 + kh;   // index among the softmax warps
     const int lbase = q4 * 32;
     const int cq = lane & 3;
     const int rA = 16 * q4 + (lane >> 2), rB = rA + 8;  // problem rows
@@ -641,14 +648,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c2 = p.softmax_scale * s_kv * 1.4426950408889634f;
     float mA = kMaxSentinel, mB = kMaxSentinel;
     float lA = 0.f, lB = 0.f;
-    // receive slot of this warp's rows: 6 KB a warp, 3 KB a warp under the key split
-    const uint32_t my_recv = sbase + L::OFF_RECV + sw * (RECV_W / 2) * NH;
+    const uint32_t my_recv = sbase + L::OFF_RECV + sw * RECV_W;  // this warp's receive slot
     const uint32_t peer_recv = ptx::mapa(my_recv, peer);
     const uint32_t peer_free = ptx::mapa(sbase + L::OFF_XFREE + sw * 4, peer);
     const uint32_t recv_full = ptx::smem_u32(&bars.recv_full[sw]);
     const uint32_t recv_free = ptx::smem_u32(&bars.recv_free[sw]);
-    // key split: this warp's and the other warp's slot of the exchange area
-    auto xslot = [&](int i, int w) { return sbase + L::OFF_XMAX + (i * 2 + w) * 512 + lane * 16; };
+    // slot i of warp w (key half) of this quarter in the exchange area
+    auto xslot = [&](int i, int w) {
+      return sbase + L::OFF_XMAX + ((q4 * 3 + i) * 2 + w) * 512 + lane * 16;
+    };
+    const uint32_t xchg0 = ptx::smem_u32(&bars.xchg[q4][0]);  // tile parity i at xchg0 + 8 i
+    const uint32_t xchg_end = ptx::smem_u32(&bars.xchg[q4][2]);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
@@ -660,19 +670,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t scol = tmem + lanes16 + TM_S + buf * T;
-      // s[32 hh + 4 j + e]: the warp's key half hh (key half kh under the
-      // key split), 8-key group j; e = 0, 1 -> row A keys 8j + 2cq + e;
-      // e = 2, 3 -> row B
-      float s[32 * NH];
+      // s[4 j + e]: 8-key group j of the key half; e = 0, 1 -> row A keys
+      // 64 kh + 8j + 2cq + e; e = 2, 3 -> row B
+      float s[32];
       {
-        uint32_t raw[NH][32];
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) ptx::tmem_ld16x256b_x8(scol + (kKS ? kh : hh) * 64, raw[hh]);
+        uint32_t raw[32];
+        ptx::tmem_ld16x256b_x8(scol + kh * 64, raw);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int hh = 0; hh < NH; ++hh)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * hh + i] = __uint_as_float(raw[hh][i]);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(raw[i]);
       }
       // Swap partial scores with the same warp of the partner CTA (single
       // receive buffer: tile t goes once the partner has read tile t - 1).
@@ -684,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t dst = peer_recv + lane * 16;
         const uint32_t bar = ptx::mapa(recv_full, peer);
 #pragma unroll
-        for (int qd = 0; qd < 2 * NH; ++qd) {  // 16 scores -> 12 words -> 3 stores
+        for (int qd = 0; qd < 2; ++qd) {  // 16 scores -> 12 words -> 3 stores
           uint32_t w[12];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -698,12 +704,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       {
-        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, NH * (RECV_W / 2));
+        if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
         if (!wait_all(c, recv_full, t & 1)) { ok = false; break; }
         const uint32_t src = my_recv + lane * 16;
         uint32_t fold = 0;
 #pragma unroll
-        for (int qd = 0; qd < 2 * NH; ++qd) {
+        for (int qd = 0; qd < 2; ++qd) {
           uint32_t w[12];
 #pragma unroll
           for (int v = 0; v < 3; ++v) {
@@ -732,13 +738,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float mxA = -INFINITY, mxB = -INFINITY;
       if (all_full) {
 #pragma unroll
-        for (int j = 0; j < 8 * NH; ++j) {
+        for (int j = 0; j < 8; ++j) {
           mxA = fmaxf(mxA, fmaxf(s[4 * j], s[4 * j + 1]));
           mxB = fmaxf(mxB, fmaxf(s[4 * j + 2], s[4 * j + 3]));
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 8 * NH; ++j)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int k = 64 * kh + 8 * j + 2 * cq + e;
@@ -750,18 +756,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
       mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-      // Key split: the two warps of the quarter trade their half-tile maxima
-      // and their sums so far (the same lane holds the same rows in both),
-      // so that both take the same rescale decisions and keep one running
-      // max.  Two slots by tile parity: a warp writes slot t % 2 again only
-      // after the other has passed tile t + 1's exchange, so after it read
-      // tile t's values.
-      float olA = 0.f, olB = 0.f;
-      if constexpr (kKS) {
+      // The two warps of the quarter trade their half-tile maxima and their
+      // sums so far (the same lane holds the same rows in both), so that
+      // both take the same rescale decisions and keep one running max.  Two
+      // slots by tile parity: a warp writes slot t % 2 again only after the
+      // other has passed tile t + 1's exchange, so after it read tile t's
+      // values.
+      float olA, olB;
+      {
         st_shared_u4(xslot(buf, kh), make_uint4(__float_as_uint(mxA), __float_as_uint(mxB),
                                                 __float_as_uint(lA), __float_as_uint(lB)));
-        ptx::mbar_arrive(ptx::smem_u32(&bars.xchg[buf]));
-        if (!wait_all(c, ptx::smem_u32(&bars.xchg[buf]), (t >> 1) & 1)) { ok = false; break; }
+        ptx::mbar_arrive(xchg0 + 8 * buf);
+        if (!wait_all(c, xchg0 + 8 * buf, (t >> 1) & 1)) { ok = false; break; }
         const uint4 o = ld_shared_u4(xslot(buf, kh ^ 1));
         mxA = fmaxf(mxA, __uint_as_float(o.x));
         mxB = fmaxf(mxB, __uint_as_float(o.y));
@@ -783,7 +789,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!wait_all(c, ptx::smem_u32(&bars.o_done), (t - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int ch = 2 * kh; ch < (kKS ? 2 * kh + 2 : 4); ++ch) {
+          for (int ch = 2 * kh; ch < 2 * kh + 2; ++ch) {
             uint32_t o[32];
             const uint32_t col = tmem + lanes16 + TM_O + ch * 64;
             ptx::tmem_ld16x256b_x8(col, o);
@@ -804,13 +810,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float nmA = -mA, nmB = -mB;
       float sA = 0.f, sB = 0.f;
       const uint32_t pcol = tmem + lanes16 + TM_S + buf * T;
-#pragma unroll
-      for (int hh = 0; hh < NH; ++hh) {
-        const int hf = kKS ? kh : hh;  // the key half in the tile
+      {
         uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int j8 = 0; j8 < 8; ++j8) {
-          const int j = 8 * hh + j8, k = 64 * hf + 8 * j8 + 2 * cq;
+        for (int j = 0; j < 8; ++j) {
+          const int k = 64 * kh + 8 * j + 2 * cq;
           float a0 = fast_exp2(fmaf(s[4 * j], c2, nmA));
           float a1 = fast_exp2(fmaf(s[4 * j + 1], c2, nmA));
           float b0 = fast_exp2(fmaf(s[4 * j + 2], c2, nmB));
@@ -823,25 +827,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           sA += a0 + a1;
           sB += b0 + b1;
-          hi[2 * j8] = kFp8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
-          hi[2 * j8 + 1] = kFp8 ? pack_f16(b0, b1) : pack_bf16(b0, b1);
+          hi[2 * j] = kFp8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+          hi[2 * j + 1] = kFp8 ? pack_f16(b0, b1) : pack_bf16(b0, b1);
           if (!kFp8) {
-            lo[2 * j8] = pack_bf16(a0 - __uint_as_float(hi[2 * j8] << 16),
-                                   a1 - __uint_as_float(hi[2 * j8] & 0xFFFF0000u));
-            lo[2 * j8 + 1] = pack_bf16(b0 - __uint_as_float(hi[2 * j8 + 1] << 16),
-                                       b1 - __uint_as_float(hi[2 * j8 + 1] & 0xFFFF0000u));
+            lo[2 * j] = pack_bf16(a0 - __uint_as_float(hi[2 * j] << 16),
+                                   a1 - __uint_as_float(hi[2 * j] & 0xFFFF0000u));
+            lo[2 * j + 1] = pack_bf16(b0 - __uint_as_float(hi[2 * j + 1] << 16),
+                                       b1 - __uint_as_float(hi[2 * j + 1] & 0xFFFF0000u));
           }
         }
-        ptx::tmem_st16x128b_x8(pcol + hf * 32, hi);
-        if (!kFp8) ptx::tmem_st16x128b_x8(pcol + T / 2 + hf * 32, lo);
+        ptx::tmem_st16x128b_x8(pcol + kh * 32, hi);
+        if (!kFp8) ptx::tmem_st16x128b_x8(pcol + T / 2 + kh * 32, lo);
       }
       lA += sA;
       lB += sB;
       if constexpr (!kFp8) {
         // The low-order terms are written for every tile; the second PV runs
-        // only where one key carries more than 1/16 of a row's weight.  Under
-        // the key split the row's sum counts the other warp's keys up to the
-        // previous tile only, which errs towards the second PV.
+        // only where one key carries more than 1/16 of a row's weight.  The
+        // row's sum counts the other warp's keys up to the previous tile
+        // only, which errs towards the second PV.
         const float pmA = limA > 0 ? fast_exp2(mtA - mA) : 0.f;
         const float pmB = limB > 0 ? fast_exp2(mtB - mB) : 0.f;
         float rsA = lA + olA * alA, rsB = lB + olB * alB;
@@ -858,18 +862,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue ---
-    if constexpr (kKS) {
-      // the other warp's share of the row sums
-      if (ok) {
-        st_shared_u4(xslot(2, kh), make_uint4(__float_as_uint(lA), __float_as_uint(lB), 0u, 0u));
-        ptx::mbar_arrive(ptx::smem_u32(&bars.xchg[2]));
-        if (wait_all(c, ptx::smem_u32(&bars.xchg[2]), 0)) {
-          const uint4 o = ld_shared_u4(xslot(2, kh ^ 1));
-          lA += __uint_as_float(o.x);
-          lB += __uint_as_float(o.y);
-        } else {
-          ok = false;
-        }
+    if (ok) {  // the other warp's share of the row sums
+      st_shared_u4(xslot(2, kh), make_uint4(__float_as_uint(lA), __float_as_uint(lB), 0u, 0u));
+      ptx::mbar_arrive(xchg_end);
+      if (wait_all(c, xchg_end, 0)) {
+        const uint4 o = ld_shared_u4(xslot(2, kh ^ 1));
+        lA += __uint_as_float(o.x);
+        lB += __uint_as_float(o.y);
+      } else {
+        ok = false;
       }
     }
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
@@ -883,7 +884,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const size_t pA = part * p.rows + rA;  // problem rows (TMEM lanes are spread)
       const size_t pB = part * p.rows + rB;
 #pragma unroll 1
-      for (int ch = 2 * kh; ch < (kKS ? 2 * kh + 2 : 4); ++ch) {
+      for (int ch = 2 * kh; ch < 2 * kh + 2; ++ch) {
         uint32_t o[32];
         ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_O + ch * 64, o);
         ptx::tmem_ld_wait();
@@ -918,7 +919,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------ teardown ---
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == Warps<kWide>::mma) {
     if (bars.abort) {
       if (lane == 0) {
         ptx::mma_commit(ptx::smem_u32(&bars.drain));
@@ -940,19 +941,19 @@ bool mla_small_rows_fit(int rows, int kv_dtype) {
 
 int mla_launch_fwd_small_sm103(const mla::FwdParams& p, void* stream) {
   const bool fp8 = p.kv_dtype == MLA_KV_FP8_E4M3;
-  const bool ks = p.rows <= 16;  // the rows fit one TMEM lane quarter: split the keys
-  auto kernel = fp8 ? (ks ? fwd_small_kernel<true, true> : fwd_small_kernel<true, false>)
-                    : (ks ? fwd_small_kernel<false, true> : fwd_small_kernel<false, false>);
+  const bool wide = p.rows > 16;  // more than lane quarter 0 holds rows (bf16 only)
+  auto kernel = fp8 ? fwd_small_kernel<true, false>
+                    : (wide ? fwd_small_kernel<false, true> : fwd_small_kernel<false, false>);
   const int smem = fp8 ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, (fp8 ? 4 : 3) + (ks ? 2 : 0));
+  e = mla::opt_in_smem(reinterpret_cast<const void*>(kernel), smem, dev, fp8 ? 4 : (wide ? 5 : 3));
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.units != nullptr ? dim3(2 * p.unit_capacity, 1, 1)
                                   : dim3(2, p.batch, p.num_splits);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(32 * (wide ? Warps<true>::count : Warps<false>::count), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];

@@ -118,6 +118,23 @@ def test_split_count_invariance_few_rows(kv_dtype, heads, sq):
 
 
 @pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
+@pytest.mark.parametrize("heads,sq", [(8, 2), (5, 3), (1, 1), (2, 8), (16, 1)])
+def test_key_split_rows(kv_dtype, heads, sq):
+    """At most 16 rows: the few-row kernel's key-split form, where the two
+    warps of TMEM lane quarter 0 share every 128-key tile and trade row maxima
+    and sums.  Causal masks across the query tokens, contexts with partial
+    tiles and parts (129, 70, 31), one shorter than Sq, 1 to many splits, and
+    outlier rows that make the running max jump."""
+    p = syn.make_problem(4, sq, heads, [1000, 129, 70, max(sq - 1, 0)], 16, kv_dtype, sq > 1,
+                         seed=50 + 7 * heads + sq, outlier_frac=0.02, name=f"key_split_h{heads}_sq{sq}")
+    ref_o, ref_l = oracle_full(p)
+    for num_sms in (2, 148, 4000):
+        out, lse, plan, st = run_gpu(p, num_sms=num_sms)
+        assert plan.key_tile == 128 and st == 0
+        assert_close(out, lse, ref_o, ref_l, f"{p.name} splits={plan.num_splits}")
+
+
+@pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
 def test_rescale_while_earlier_pv_in_flight_few_rows(kv_dtype):
     p = _growing_rope(kv_dtype, [0.2, 0.2, 6.0, 6.0, 12.0, 12.0, 18.0, 18.0, 24.0, 24.0, 1.0, 1.0],
                       heads=16)
@@ -304,6 +321,13 @@ def test_full_fp8_long_ctx109440():
 
 @pytest.mark.parametrize("heads,sq,ps", [(16, 8, 64), (64, 2, 1), (32, 4, 16), (16, 4, 64)])
 def test_full_mtp_causal(heads, sq, ps):
+    full_check(syn.mtp(heads, sq, ps))
+
+
+@pytest.mark.parametrize("heads,sq,ps", [(16, 1, 64), (8, 2, 16)])
+def test_full_mtp_recipe_key_split(heads, sq, ps):
+    """The MTP recipe (causal, outlier rows) at 16 rows: the key-split form
+    with a bf16 cache at full size."""
     full_check(syn.mtp(heads, sq, ps))
 
 
