@@ -146,7 +146,7 @@ constexpr uint32_t kSleepNs = 20000;
 
 struct Bars {
   uint64_t kv_full[NS];   // every loader part of the stage landed (32 lanes a part)
-  uint64_t kv_empty[NS];  // the stage's MMAs are done
+  uint64_t kv_empty[NS][4];  // a loader part's rows of the stage are read for the last time
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t recv_full[8];  // per softmax warp
@@ -335,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars.kv_full[s]), 32 * UPT);
-      ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s]), 1);
+      for (int h = 0; h < 4; ++h) ptx::mbar_init(ptx::smem_u32(&bars.kv_empty[s][h]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.s_full[i]), 1);
@@ -387,17 +387,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
       };
       auto issue_pv = [&](int t, bool second) {
+        const int s = t % NS;
         const uint32_t pa = tmem + TM_S + (t & 1) * T;
-        const uint32_t st = sbase + L::OFF_STAGE + (t % NS) * STAGE;
-        for (int kk = 0; kk < T / 16; ++kk)
+        const uint32_t st = sbase + L::OFF_STAGE + s * STAGE;
+        const bool two = !kFp8 && second;
+        constexpr int MPP = PART / 16;  // value MMAs (16 keys each) per loader part
+        for (int kk = 0; kk < T / 16; ++kk) {
           ptx::mma_ts(tmem + TM_O, pa + kk * 8, vdesc(st + kk * 2048), id_pv, (t | kk) != 0);
-        if (!kFp8 && second) {
+          // the part's rows are read for the last time (the score MMAs of
+          // this tile are long done): its loader may refill them
+          if (!two && kk % MPP == MPP - 1) ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[s][kk / MPP]));
+        }
+        if (two) {
           for (int kk = 0; kk < T / 16; ++kk)
             ptx::mma_ts(tmem + TM_O, pa + T / 2 + kk * 8, vdesc(st + kk * 2048), id_pv, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
         if (t == n_tiles - 1) ptx::mma_commit(ptx::smem_u32(&bars.o_final));
-        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
+        if (two)
+          for (int h = 0; h < UPT; ++h) ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[s][h]));
       };
       int nq = 0, np = 0;
       uint64_t t_last = ptx::globaltimer_ns();
@@ -501,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         rows_of(u);
         load_pages(u + kLoaders);
         const uint32_t stage = sbase + L::OFF_STAGE + s * STAGE;
-        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) break;
+        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s][h]), ((t / NS) - 1) & 1)) break;
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
           const int kk = h * PART + i * IPI + g;  // key within the tile
@@ -545,7 +553,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         ptx::cp_async_commit();
         ptx::cp_async_wait<1>();  // this lane's copies of part u have landed
         const int t = u / UPT, h = u % UPT, s = t % NS;
-        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s]), ((t / NS) - 1) & 1)) break;
+        if (t >= NS && !wait_all(c, ptx::smem_u32(&bars.kv_empty[s][h]), ((t / NS) - 1) & 1)) break;
         // e4m3 codes -> f16 operands (exact); the per-tensor scale goes to
         // the scores and the output instead.  A lane converts the codes it
         // copied.
