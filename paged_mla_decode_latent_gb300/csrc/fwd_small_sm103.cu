@@ -69,7 +69,9 @@ struct LoadPart {
   static constexpr int keys = kFp8 ? 32 : 64;  // keys of one loader part
 };
 constexpr int RAW_PART = 32 * (256 + 32);      // fp8 codes of a 32-key part: 9 KB
-constexpr int NR = 6;                          // raw slots (two per loader warp)
+// Raw slots: two for each loader warp but the first, which owns a tile's
+// first part (the first the value MMAs release) and has one.
+constexpr int NR = 7;
 // Rows and warps: a warp reaches only the TMEM lane quarter warp % 4, and
 // each quarter belongs to one SM sub-partition.  So that all four
 // sub-partitions share the softmax, the (at most 64) rows are spread 16 to a
@@ -81,22 +83,26 @@ constexpr int NR = 6;                          // raw slots (two per loader warp
 // maxima and sums through shared memory, so a softmax warp holds 32 scores a
 // thread.  Two forms:
 //   narrow (at most 16 rows, quarter 0 only): 8 warps; 0 and 4 softmax,
-//     1-3 load, 5 and 6 idle, 7 issues the MMAs;
+//     6, 1, 2, 3 load (loader index 0..3, so with 32-key parts warp 1 + i
+//     owns part i of every tile and the two parts that share a sub-partition
+//     are released first and third), 5 idle, 7 issues the MMAs;
 //   wide (17 to 64 rows, bf16): 12 warps; 0-7 softmax (two per quarter),
 //     8-10 load, 11 issues the MMAs (168 registers a thread).
-constexpr int kLoaders = 3;
 template <bool kWide>
 struct Warps {
   static constexpr int count = kWide ? 12 : 8;
   static constexpr int softmax = kWide ? 8 : 2;
+  static constexpr int loaders = kWide ? 3 : 4;
   static constexpr int mma = kWide ? 11 : 7;
 };
 template <bool kWide>
 __device__ __forceinline__ bool is_softmax_warp(int w) { return kWide ? w < 8 : (w == 0 || w == 4); }
 template <bool kWide>
-__device__ __forceinline__ bool is_loader_warp(int w) { return kWide ? (w >= 8 && w <= 10) : (w >= 1 && w <= 3); }
+__device__ __forceinline__ bool is_loader_warp(int w) {
+  return kWide ? (w >= 8 && w <= 10) : ((w >= 1 && w <= 3) || w == 6);
+}
 template <bool kWide>
-__device__ __forceinline__ int loader_index(int w) { return kWide ? w - 8 : w - 1; }
+__device__ __forceinline__ int loader_index(int w) { return kWide ? w - 8 : (w == 6 ? 0 : w); }
 __device__ __forceinline__ int mma_row(int r) { return 32 * (r >> 4) + (r & 15); }
 constexpr int RECV_W = 32 * 16 * 6;     // one warp's partial scores: 16 rows x 64 keys x 3 B (3 KB)
 
@@ -466,6 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
     const char* cache = static_cast<const char*>(p.cache);
     const int n_units = UPT * n_tiles;
     const int lw = loader_index<kWide>(warp);
+    constexpr int kLoaders = Warps<kWide>::loaders;
     // i-th key of this lane in part u, clamped to the split's last key k1 - 1:
     // a partial part, or the empty parts of a split's last tile, repeat a real
     // row (its weights are masked to zero), so every key read lies in
@@ -525,8 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
       }
     } else {
-      // raw slot j of this warp: [PART keys][288 codes]
-      auto raw_slot = [&](int j) { return sbase + L::OFF_RAW + (2 * lw + j) * RAW_PART; };
+      // raw slot j of this warp: [PART keys][288 codes]; loader 0 has one
+      const int nslot = lw == 0 ? 1 : 2;
+      auto raw_slot = [&](int j) { return sbase + L::OFF_RAW + (lw == 0 ? 0 : 2 * lw - 1 + j) * RAW_PART; };
       auto issue_raw = [&](int u, int j) {
         rows_of(u);
         const uint32_t raw = raw_slot(j);
@@ -544,9 +552,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
       ptx::cp_async_commit();
       load_pages(lw + kLoaders);
       int j = 0;
-      for (int u = lw; u < n_units; u += kLoaders, j ^= 1) {
+      for (int u = lw; u < n_units; u += kLoaders, j ^= nslot - 1) {
         const int un = u + kLoaders;
-        if (un < n_units) {
+        if (nslot == 2 && un < n_units) {
           issue_raw(un, j ^ 1);
           load_pages(un + kLoaders);
         }
@@ -594,11 +602,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(ptx::smem_u32(&bars.kv_full[s]));
+        if (nslot == 1 && un < n_units) {  // its one slot is free again
+          issue_raw(un, 0);
+          load_pages(un + kLoaders);
+          ptx::cp_async_commit();
+        }
       }
     }
     ptx::cp_async_wait<0>();
   } else if (!is_softmax_warp<kWide>(warp)) {
-    // warps 5 and 6 of the narrow form: no work
+    // warp 5 of the narrow form: no work
   } else {
     // ----------------------------------------------------------- softmax ---
     // As in the 128-row kernel's 16x256b access: warp q owns TMEM lanes
