@@ -14,7 +14,7 @@
 // chunk storing its own slice.
 //
 // GB300 form: a CTA takes 128 tokens of one sequence (the MMA M) and a group
-// of up to kGroup heads.  The 128 gathered latent rows go into TMEM as the A
+// of up to kGroup heads (fewer when that leaves SMs idle: see the launcher).  The 128 gathered latent rows go into TMEM as the A
 // operand (256 columns of bf16 pairs; fp8 codes converted exactly on the
 // way), so shared memory holds only the weights: each (head, key or value
 // half) unit's 128 x 512 block streams through a ring of twelve 64-dim
@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "../../include/mla_decode.h"
@@ -85,6 +86,7 @@ struct GkvParams {
   uint16_t* v_out;    // bf16 [T, H, 128]
   int32_t* status;
   int page_size, fp8, heads, max_ctx;
+  int group;  // heads per CTA
 };
 
 struct Ctx {
@@ -145,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
   const int j0 = chunk * kTok;
   if (j0 >= ctx) return;  // past this sequence's last chunk
   const int n_tok = min(kTok, ctx - j0);
-  const int h0 = group * kGroup;
-  const int n_heads = min(kGroup, p.heads - h0);
+  const int h0 = group * p.group;
+  const int n_heads = min(p.group, p.heads - h0);
   const int n_units = 2 * n_heads;  // (head, keys or values)
   const int n_slabs = n_units * kSlabs;
   const int64_t t0 = (int64_t)p.cu_seqlens[b] + j0;
@@ -446,13 +448,33 @@ extern "C" int mla_gather_kv_b_proj(const void* kv_cache, int64_t num_pages, int
   p.fp8 = kv_dtype == MLA_KV_FP8_E4M3;
   p.heads = num_heads;
   p.max_ctx = max_ctx;
-  int dev = 0;
+  int dev = 0, num_sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (mla::opt_in_smem(reinterpret_cast<const void*>(gather_kvb_kernel), SMEM_BYTES, dev, 2) !=
       cudaSuccess)
     return MLA_ERR_CUDA;
+  // Heads per CTA.  A CTA's (head, keys / values) units run one after the
+  // other, so its time is about (gather + g heads) and the launch takes
+  // ceil(CTAs / SMs) such rounds (one CTA per SM).  Few chunks (short
+  // contexts) leave most SMs idle with all heads in one CTA; smaller groups
+  // spread the heads, each CTA gathering the same rows again (from L2).
+  // The cost is counted in heads, the gather and fill taken as half a head.
+  const int64_t chunks = (int64_t)((max_ctx + kTok - 1) / kTok) * batch;
+  int group = std::min(kGroup, num_heads);
+  double best = 1e300;
+  for (int g = std::min(kGroup, num_heads); g >= 1; --g) {
+    const int64_t ctas = chunks * ((num_heads + g - 1) / g);
+    const double t = (double)((ctas + num_sms - 1) / num_sms) * (0.5 + g);
+    if (t < best * 0.97) {  // a smaller group only for a clear gain
+      best = t;
+      group = g;
+    }
+  }
+  p.group = group;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_ctx + kTok - 1) / kTok, (num_heads + kGroup - 1) / kGroup, batch);
+  cfg.gridDim = dim3((max_ctx + kTok - 1) / kTok, (num_heads + group - 1) / group, batch);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
