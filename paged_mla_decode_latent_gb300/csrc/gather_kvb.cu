@@ -18,21 +18,24 @@
 // operand (256 columns of bf16 pairs; fp8 codes converted exactly on the
 // way), so shared memory holds only the weights: each (head, key or value
 // half) unit's 128 x 512 block streams through a ring of twelve 64-dim
-// slabs (16 KB each, the B operand, K-major 128B-swizzled), about 192 KB in
-// flight.  tcgen05 MMAs (M = 128, N = 128, K = 16, A from TMEM) accumulate a
+// slabs (16 KB each, the B operand, K-major 128B-swizzled), each one TMA tile
+// load of the weight tensor, about 192 KB in flight.  tcgen05 MMAs (M = 128, N = 128, K = 16, A from TMEM) accumulate a
 // unit in one of two 128-column TMEM accumulators while four epilogue warps
 // drain the other (fp32 -> bf16, x kv_scale for fp8).
 //
-// Warps: 0-2 weight loaders (each keeps four slabs in flight), 3 MMA issue,
+// Warps: 0 weight loads (one thread issues the TMA loads), 1-2 idle, 3 MMA issue,
 // 4-7 gather the rows into TMEM, write the rope dims and drain the
 // accumulators (TMEM lane quarters 0-3).  Every wait is bounded (2 s): a
 // wait that runs out sets MLA_DEVFLAG_TIMEOUT and the CTA winds down.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/mla_decode.h"
 #include "internal.h"
@@ -45,9 +48,7 @@ constexpr int kUnitN = 128;         // outputs per unit (MMA N): a head's keys o
 constexpr int kLatent = 512;        // contraction (MMA K over 8 slabs)
 constexpr int kSlabs = kLatent / 64;
 constexpr int kGroup = 16;          // heads per CTA (the gathered rows serve them all)
-constexpr int kLoaders = 3;
-constexpr int kInFlight = 4;        // slabs a loader warp keeps in flight
-constexpr int kStages = kLoaders * kInFlight;  // 12
+constexpr int kStages = 12;         // weight slabs in flight (16 KB each)
 constexpr int B_SLAB = kUnitN * 128;           // 16 KB
 constexpr int OFF_B = 0;
 constexpr int STG_W = 32 * 256;                    // a warp's 32 output rows of 256 B
@@ -60,6 +61,7 @@ constexpr int kThreads = 32 * 8;
 constexpr uint32_t TM_A = 0;    // 256 columns: the 512 latent dims as bf16 pairs
 constexpr uint32_t TM_D = 256;  // two 128-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 500000000ull;
 
 struct Bars {
   uint64_t a_full;            // rows in TMEM (128 gather threads)
@@ -129,7 +131,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // K-major, 128B-swizzled operand: rows 128 B apart, 8-row groups 1 KB apart.
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return ptx::smem_desc(addr, 16, 1024, 2); }
 
-__global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    gather_kvb_kernel(GkvParams p, const __grid_constant__ CUtensorMap wmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars.a_full), 128);
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars.b_full[s]), 32);
+      ptx::mbar_init(ptx::smem_u32(&bars.b_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars.b_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -178,47 +181,36 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
   const uint32_t tmem = bars.tmem_base;
   Ctx c{p.status, &bars.abort};
 
-  if (warp < kLoaders) {
-    // ------------------------------------------------- weight loaders ---
-    // Loader warp w fills slabs i = w, w + 3, ... (slab k = i % 8 of unit
-    // i / 8: 128 weight rows x 64 dims) into stage i % 12, which it owns:
-    // 16-byte cp.async pieces into the 128B-swizzled K-major layout, one
-    // commit group per slab, four groups in flight; when a group is done the
-    // lanes fence it for the tensor cores and arrive on its stage's barrier.
-    int pend[kInFlight];
-    int n_pend = 0, head = 0;
-    bool ok = true;
-    for (int i = warp; i < n_slabs; i += kLoaders) {
-      const int s = i % kStages;
-      if (i >= kStages && !wait_all(c, ptx::smem_u32(&bars.b_empty[s]), ((i / kStages) - 1) & 1)) {
-        ok = false;
-        break;
+  if (warp == 0) {
+    // ------------------------------------------------- weight loader ---
+    // One thread fills slab i (slab k = i % 8 of unit i / 8: 128 weight rows
+    // x 64 dims) into stage i % 12 with one TMA tile load (the map's 128-byte
+    // swizzle gives the K-major operand layout), counted on the stage's
+    // barrier; a stage is refilled once the MMAs that read it are done.
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_slabs; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages && !wait(c, ptx::smem_u32(&bars.b_empty[s]), ((i / kStages) - 1) & 1)) break;
+        const int unit = i / kSlabs, k = i % kSlabs;
+        const int h = h0 + (unit >> 1), x = unit & 1;
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bars.b_full[s]), B_SLAB);
+        ptx::tma_load_2d(sbase + OFF_B + s * B_SLAB, &wmap, k * 64, h * 256 + x * kUnitN,
+                         ptx::smem_u32(&bars.b_full[s]));
+        ++issued;
       }
-      const int unit = i / kSlabs, k = i % kSlabs;
-      const int h = h0 + (unit >> 1), x = unit & 1;
-      const uint16_t* src = p.w + ((size_t)h * 256 + x * kUnitN) * kLatent + k * 64;
-      const uint32_t dst = sbase + OFF_B + s * B_SLAB;
-#pragma unroll 4
-      for (int q = lane; q < kUnitN * 8; q += 32) {
-        const int o = q >> 3, piece = q & 7;
-        ptx::cp_async_16(dst + o * 128 + ((piece ^ (o & 7)) * 16), src + (size_t)o * kLatent + piece * 8);
-      }
-      ptx::cp_async_commit();
-      pend[(head + n_pend) % kInFlight] = s;
-      if (++n_pend == kInFlight) {
-        ptx::cp_async_wait<kInFlight - 1>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(ptx::smem_u32(&bars.b_full[pend[head]]));
-        head = (head + 1) % kInFlight;
-        --n_pend;
+      // No copy may still be landing when the CTA leaves (after a wind-down
+      // the MMA warp may not have consumed them): wait for the last ones.
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+        const uint32_t bar = ptx::smem_u32(&bars.b_full[i % kStages]);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, (i / kStages) & 1))
+          if (ptx::globaltimer_ns() - t0 > kDrainNs) break;
       }
     }
-    ptx::cp_async_wait<0>();
-    if (ok) {
-      ptx::fence_proxy_async_smem();
-      for (; n_pend > 0; --n_pend, head = (head + 1) % kInFlight)
-        ptx::mbar_arrive(ptx::smem_u32(&bars.b_full[pend[head]]));
-    }
+    __syncwarp();
+  } else if (warp < kMmaWarp) {
+    // warps 1 and 2: no work
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA ---
     if (lane == 0) {
@@ -410,6 +402,25 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kvb_kernel(GkvParams p) {
 
 }  // namespace
 
+namespace {
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static void* fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+  });
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+}  // namespace
+
 extern "C" int mla_gather_kv_b_proj(const void* kv_cache, int64_t num_pages, int32_t page_size,
                                     int32_t kv_dtype, const float* kv_scale,
                                     const int32_t* block_table, int64_t bt_stride,
@@ -473,6 +484,20 @@ extern "C" int mla_gather_kv_b_proj(const void* kv_cache, int64_t num_pages, int
     }
   }
   p.group = group;
+  // The weights [H, 256, 512] as a 2-D tensor of H * 256 rows of 512 bf16,
+  // read in boxes of 128 rows x 64 dims with the 128-byte swizzle of the
+  // K-major operand.
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return MLA_ERR_CUDA;
+  CUtensorMap wmap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kLatent, (cuuint64_t)num_heads * 256};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kLatent * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kUnitN};
+  const cuuint32_t estride[2] = {1, 1};
+  if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_kv_b), gdim, gstride,
+             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((max_ctx + kTok - 1) / kTok, (num_heads + group - 1) / group, batch);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -483,6 +508,6 @@ extern "C" int mla_gather_kv_b_proj(const void* kv_cache, int64_t num_pages, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gather_kvb_kernel, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, gather_kvb_kernel, p, wmap) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
