@@ -38,7 +38,8 @@
 //   MMA warp      : S_part = Q_part K_part^T (18 MMAs, N = 128, A = Q from
 //                   shared memory), then O_half += P V_half (8 MMAs, N =
 //                   256, A = P from TMEM, B = the same stage read MN-major;
-//                   8 more with the low-order weights on heavy tiles).
+//                   up to 8 more with the low-order weights, one for each
+//                   16-key group that holds a heavy key).
 //   softmax warps : as in the 128-row kernel, two warps per 16-row quarter,
 //                   each over one 64-key half of the tile: 32 scores a
 //                   thread, 3 KB swapped per warp and tile, row maxima and
@@ -392,11 +393,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
                       id_qk, 1);
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
       };
-      auto issue_pv = [&](int t, bool second) {
+      // heavy: bit kk asks for the low-order weights of the tile's 16-key group kk
+      auto issue_pv = [&](int t, uint32_t heavy) {
         const int s = t % NS;
         const uint32_t pa = tmem + TM_S + (t & 1) * T;
         const uint32_t st = sbase + L::OFF_STAGE + s * STAGE;
-        const bool two = !kFp8 && second;
+        const bool two = !kFp8 && heavy != 0;
         constexpr int MPP = PART / 16;  // value MMAs (16 keys each) per loader part
         for (int kk = 0; kk < T / 16; ++kk) {
           ptx::mma_ts(tmem + TM_O, pa + kk * 8, vdesc(st + kk * 2048), id_pv, (t | kk) != 0);
@@ -406,7 +408,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         }
         if (two) {
           for (int kk = 0; kk < T / 16; ++kk)
-            ptx::mma_ts(tmem + TM_O, pa + T / 2 + kk * 8, vdesc(st + kk * 2048), id_pv, 1);
+            if ((heavy >> kk) & 1u)
+              ptx::mma_ts(tmem + TM_O, pa + T / 2 + kk * 8, vdesc(st + kk * 2048), id_pv, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
         if (t == n_tiles - 1) ptx::mma_commit(ptx::smem_u32(&bars.o_final));
@@ -426,8 +429,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
         }
         if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1)) {
           ptx::tc_fence_after();
-          const bool second = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[np & 1]) != 0;
-          issue_pv(np++, second);
+          const uint64_t hv = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[np & 1]);
+          uint32_t heavy = 0;  // the OR of the softmax warps' bytes
+          for (int i = 0; i < 8; ++i) heavy |= (uint32_t)(hv >> (8 * i)) & 0xFFu;
+          issue_pv(np++, heavy);
           progress = true;
         }
         if (progress) {
@@ -831,6 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
       const float nmA = -mA, nmB = -mB;
       float sA = 0.f, sB = 0.f;
       const uint32_t pcol = tmem + lanes16 + TM_S + buf * T;
+      float gA[4] = {0.f, 0.f, 0.f, 0.f}, gB[4] = {0.f, 0.f, 0.f, 0.f};  // per 16-key group
       {
         uint32_t hi[16], lo[16];
 #pragma unroll
@@ -848,6 +854,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
           }
           sA += a0 + a1;
           sB += b0 + b1;
+          if (!kFp8) {
+            gA[j >> 1] = fmaxf(gA[j >> 1], fmaxf(a0, a1));
+            gB[j >> 1] = fmaxf(gB[j >> 1], fmaxf(b0, b1));
+          }
           hi[2 * j] = kFp8 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
           hi[2 * j + 1] = kFp8 ? pack_f16(b0, b1) : pack_bf16(b0, b1);
           if (!kFp8) {
@@ -864,18 +874,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
       lB += sB;
       if constexpr (!kFp8) {
         // The low-order terms are written for every tile; the second PV runs
-        // only where one key carries more than 1/16 of a row's weight.  The
-        // row's sum counts the other warp's keys up to the previous tile
-        // only, which errs towards the second PV.
-        const float pmA = limA > 0 ? fast_exp2(mtA - mA) : 0.f;
-        const float pmB = limB > 0 ? fast_exp2(mtB - mB) : 0.f;
+        // only over the 16-key groups where one key carries more than 1/16
+        // of a row's weight.  The row's sum counts the other warp's keys up
+        // to the previous tile only, which errs towards the second PV.  Bit
+        // g of this warp's byte is group 4 kh + g of the tile.
         float rsA = lA + olA * alA, rsB = lB + olB * alB;
         rsA += __shfl_xor_sync(0xffffffffu, rsA, 1);
         rsB += __shfl_xor_sync(0xffffffffu, rsB, 1);
         rsA += __shfl_xor_sync(0xffffffffu, rsA, 2);
         rsB += __shfl_xor_sync(0xffffffffu, rsB, 2);
-        const bool heavy = __any_sync(0xffffffffu, pmA * 16.f > rsA || pmB * 16.f > rsB);
-        if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = heavy ? 1 : 0;
+        uint32_t gm = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (gA[g] * 16.f > rsA || gB[g] * 16.f > rsB) gm |= 1u << g;
+        gm = __reduce_or_sync(0xffffffffu, gm);
+        if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[buf])[sw] = (uint8_t)(gm << (4 * kh));
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
