@@ -28,13 +28,15 @@
 // softmax in the softmax warps whose 16-row block holds real rows.
 //
 // Per 128-key tile:
-//   loader warps  : three warps, each owning parts 3i + w of the tile
-//                   sequence (64 keys for bf16, 32 for fp8): block-table
-//                   lookup, 16-byte cp.async of the part's row pieces into
-//                   the tile's stage (bf16) or into one of the warp's two raw
-//                   slots, converted to f16 by the same lanes (fp8, the next
-//                   part's copy already in flight); every part arrives on the
-//                   stage's barrier.
+//   loader warps  : L warps (4 in the narrow form, 3 in the wide one), loader
+//                   l owning parts Li + l of the tile sequence (64 keys for
+//                   bf16, 32 for fp8): block-table lookup, 16-byte cp.async
+//                   of the part's row pieces into the tile's stage (bf16) or
+//                   into one of the loader's raw slots, converted to f16 by
+//                   the same lanes (fp8, the next part's copy already in
+//                   flight); every part arrives on the stage's barrier, and
+//                   a part's stage rows are refilled as soon as the last
+//                   value MMA that reads them is done.
 //   MMA warp      : S_part = Q_part K_part^T (18 MMAs, N = 128, A = Q from
 //                   shared memory), then O_half += P V_half (8 MMAs, N =
 //                   256, A = P from TMEM, B = the same stage read MN-major;
