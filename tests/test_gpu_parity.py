@@ -134,6 +134,38 @@ def test_key_split_rows(kv_dtype, heads, sq):
         assert_close(out, lse, ref_o, ref_l, f"{p.name} splits={plan.num_splits}")
 
 
+def _random_cases(n=24, seed=2026):
+    """Seeded random shapes over both kernels and every few-row form: heads
+    1..128, Sq 1..8 (rows up to 384, several 128-row blocks), page sizes
+    1..128, bf16 / fp8, causal or not, ragged contexts with empty and
+    shorter-than-Sq ones, sometimes outlier rows and poisoned slack."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        heads = int(rng.choice([1, 2, 3, 5, 8, 12, 16, 20, 32, 48, 64, 100, 128]))
+        sq = int(rng.integers(1, 9)) if heads * 8 <= 384 else int(rng.integers(1, 384 // heads + 1))
+        ps = int(rng.choice([1, 2, 3, 5, 16, 33, 64, 128]))
+        batch = int(rng.integers(1, 4))
+        lens = [int(x) for x in rng.integers(0, 1800, batch)]
+        if rng.random() < 0.3:
+            lens[0] = int(rng.integers(0, sq + 1))
+        kv = syn.KV_FP8_E4M3 if rng.random() < 0.4 else syn.KV_BF16
+        causal = bool(rng.random() < 0.6) and sq > 1
+        cases.append((i, heads, sq, ps, lens, kv, causal, 0.02 if rng.random() < 0.5 else 0.0,
+                      bool(rng.random() < 0.3)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: f"case{c[0]}_h{c[1]}_sq{c[2]}_ps{c[3]}")
+def test_random_shapes(case):
+    i, heads, sq, ps, lens, kv, causal, outliers, poison = case
+    p = syn.make_problem(len(lens), sq, heads, lens, ps, kv, causal, seed=300 + i,
+                         outlier_frac=outliers, poison=poison, name=f"random{i}")
+    check(p)
+    if sum(lens) > 0:  # and with a forced split count
+        check(p, num_sms=8)
+
+
 @pytest.mark.parametrize("kv_dtype", [syn.KV_BF16, syn.KV_FP8_E4M3])
 def test_rescale_while_earlier_pv_in_flight_few_rows(kv_dtype):
     p = _growing_rope(kv_dtype, [0.2, 0.2, 6.0, 6.0, 12.0, 12.0, 18.0, 18.0, 24.0, 24.0, 1.0, 1.0],
