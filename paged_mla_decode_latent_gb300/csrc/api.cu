@@ -11,6 +11,7 @@
 #include "internal.h"
 
 int mla_launch_fwd_sm103(const mla::FwdParams& p, void* stream);
+int mla_launch_fwd_pipe_sm103(const mla::FwdParams& p, void* stream);
 
 namespace {
 
@@ -201,7 +202,10 @@ cudaError_t opt_in_smem(const void* kernel, int bytes, int dev, int slot) {
 
 }  // namespace mla
 
+// Few-row blocks go to the 128-key-tile kernel; 128-row blocks with a bf16
+// cache to the four-stage kernel (fp8 needs room for raw stages it lacks).
 int mla_launch_fwd(const mla::FwdParams& p, void* stream) {
   if (p.key_tile == mla::kKeyTileSmall) return mla_launch_fwd_small_sm103(p, stream);
+  if (p.kv_dtype == MLA_KV_BF16) return mla_launch_fwd_pipe_sm103(p, stream);
   return mla_launch_fwd_sm103(p, stream);
 }

@@ -277,16 +277,18 @@ def test_context_between_max_ctx_and_split_cover(which, num_sms):
     assert_close(out, lse, ref_o, ref_l, "clamped contexts")
 
 
-@pytest.mark.parametrize("form", ["128_rows", "few_rows_fp8", "few_rows_wide_bf16", "few_rows_narrow_bf16"])
+@pytest.mark.parametrize("form", ["128_rows_bf16", "128_rows_fp8", "few_rows_fp8", "few_rows_wide_bf16", "few_rows_narrow_bf16"])
 def test_wait_limit_runs_out_without_fault(form):
     """With a 1 us bound every long wait of the pipeline gives up: the call
     reports MLA_ERR_TIMEOUT through the status word, no fault, and the next
     call with the default bound on the same workspace is correct.  For the
-    128-row kernel and each form of the few-row kernel (its key-split
+    128-row kernels (bf16 and fp8 caches) and each form of the few-row kernel (its key-split
     exchanges and part pipelines included)."""
     import ctypes
     import torch
-    p = {"128_rows": lambda: syn.dense(16, 4096, seed=40),
+    p = {"128_rows_bf16": lambda: syn.dense(16, 4096, seed=40),
+         "128_rows_fp8": lambda: syn.make_problem(16, 1, 128, [4096] * 16, 1, syn.KV_FP8_E4M3, False,
+                                                  seed=46, name="dense_h128_b16_ctx4096_fp8"),
          "few_rows_fp8": lambda: syn.fp8_long(4096, batch=4, seed=41),
          "few_rows_wide_bf16": lambda: syn.mtp(16, 4, 64, batch=4, ctx=4096, seed=42),
          "few_rows_narrow_bf16": lambda: syn.mtp(8, 2, 16, batch=4, ctx=4096, seed=43)}[form]()
