@@ -137,6 +137,7 @@ struct Ctx {
   int32_t* status;
   volatile int32_t* abort;
   uint64_t limit_ns;  // bound of every pipeline wait (FwdParams::wait_ns)
+  uint32_t sleep_ns;  // suspend hint of a wait: no longer than the limit, so any limit is reachable
 };
 
 // Wait used only while winding down after an abort: ignores the abort word,
@@ -158,9 +159,10 @@ __device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity
   while (true) {
     // Sleep on the barrier rather than spin: waiting warps would otherwise
     // take issue slots from the warps that share their sub-partition.  A
-    // failed try suspends the thread for up to kSleepNs, so reading the
-    // timer after each one costs nothing that matters.
-    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    // failed try suspends the thread for up to kSleepNs (the wait limit
+    // if that is shorter), so reading the timer after each one costs
+    // nothing that matters.
+    if (ptx::mbar_try_wait_sleep(bar, parity, c.sleep_ns)) return true;
     if (*c.abort) return false;
     if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
       atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
@@ -371,7 +373,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // when the launch is not a programmatic dependent one.
   ptx::grid_dependency_wait();
   const uint32_t tmem = bars.tmem_base;
-  Ctx c{p.status, &bars.abort, p.wait_ns};
+  Ctx c{p.status, &bars.abort, p.wait_ns,
+        (uint32_t)(p.wait_ns < (uint64_t)kSleepNs ? p.wait_ns : (uint64_t)kSleepNs)};
 
   if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---

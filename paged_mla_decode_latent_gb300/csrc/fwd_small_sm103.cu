@@ -175,6 +175,7 @@ struct Ctx {
   int32_t* status;
   volatile int32_t* abort;
   uint64_t limit_ns;
+  uint32_t sleep_ns;  // suspend hint of a wait: no longer than the limit, so any limit is reachable
 };
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
@@ -188,7 +189,7 @@ __device__ __forceinline__ bool wait(const Ctx& c, uint32_t bar, uint32_t parity
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, c.sleep_ns)) return true;
     if (*c.abort) return false;
     if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
       atomicOr(c.status, MLA_DEVFLAG_TIMEOUT);
@@ -373,7 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
   ptx::tc_fence_after();
   ptx::grid_dependency_wait();
   const uint32_t tmem = bars.tmem_base;
-  Ctx c{p.status, &bars.abort, p.wait_ns};
+  Ctx c{p.status, &bars.abort, p.wait_ns,
+        (uint32_t)(p.wait_ns < (uint64_t)kSleepNs ? p.wait_ns : (uint64_t)kSleepNs)};
 
   if (warp == Warps<kWide>::mma) {
     // --------------------------------------------------------------- MMA ---
@@ -651,11 +653,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
     {
       bool q_range = false;
       const int n_pieces = p.rows * 36;  // per row: 4 slabs x 8 chunks + 4 rope chunks
-      for (int i = sw * 32 + lane; i < n_pieces; i += 32 * NSW) {
+      // Piece i of row r: its global source and its place in shared memory.
+      auto piece = [&](int i, uint4& x, uint32_t& dst) {
         const int r = i / 36, pc = i % 36, ar = mma_row(r);
         const uint16_t* qrow = p.q + ((size_t)b * p.rows + r) * mla::kDQK;
-        uint4 x;
-        uint32_t dst;
         if (pc < 32) {
           const int sl = pc >> 3, ch = pc & 7;
           x = reinterpret_cast<const uint4*>(qrow + vdim0 + sl * 64)[ch];
@@ -665,6 +666,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Warps<kWide>::count 
           x = reinterpret_cast<const uint4*>(qrow + 512 + 32 * (int)rank)[ch];
           dst = sbase + L::OFF_Q + L::qrope_off() + sw64(ar, ch);
         }
+      };
+      // Up to kQPieces pieces a thread (every form's row limit keeps it
+      // there): every load first, then the stores, which are ordered memory
+      // operations that loads between them would each wait for.
+      constexpr int kQPieces = 9;
+      const int i0 = sw * 32 + lane, step = 32 * NSW;
+      uint4 xs[kQPieces];
+      uint32_t dsts[kQPieces];
+#pragma unroll
+      for (int k = 0; k < kQPieces; ++k)
+        if (i0 + k * step < n_pieces) piece(i0 + k * step, xs[k], dsts[k]);
+#pragma unroll
+      for (int k = 0; k < kQPieces; ++k)
+        if (i0 + k * step < n_pieces) {
+          if (kFp8) xs[k] = bf16x8_to_f16x8(xs[k], q_range);
+          st_shared_u4(dsts[k], xs[k]);
+        }
+      for (int i = i0 + kQPieces * step; i < n_pieces; i += step) {  // beyond the forms' limits
+        uint4 x;
+        uint32_t dst;
+        piece(i, x, dst);
         if (kFp8) x = bf16x8_to_f16x8(x, q_range);
         st_shared_u4(dst, x);
       }
