@@ -24,7 +24,7 @@
 // Per 64-key tile, in each CTA:
 //   loader warps 0-2 : tiles dealt round robin (warp w takes tiles w, w + 3,
 //                      ...; tile t goes to stage t % 4), 16-byte cp.async of
-//                      the CTA's latent half and rope quarter of each key;
+//                      the CTA's latent half and rope half of each key;
 //   MMA warp 3       : S = Q K^T (8 MMAs with A from TMEM, 8 + 2 with A from
 //                      shared memory; N = 64) into score buffer t % 3 once
 //                      the PV of tile t - 3 is issued; O += P V (4 MMAs, N =
