@@ -63,7 +63,7 @@ namespace {
 constexpr int T = mla::kKeyTile;       // 64 keys per tile
 constexpr int NB = 3;                  // score buffers (2 or 3)
 constexpr int QT = NB == 3 ? 2 : 4;    // 64-dim latent slabs of Q in TMEM (the rest in shared memory)
-constexpr int NS = 4;                  // operand stages
+constexpr int NS = 4;                  // operand stages (a power of two)
 constexpr int kLoaders = 3;            // loader warps (tiles dealt round robin)
 constexpr int ATOM = T * 128;          // one 64-dim latent slab of a stage: 8 KB
 constexpr int RATOM = T * 64;          // the CTA's 32 rope dims of a stage, 64-byte rows: 4 KB
@@ -93,6 +93,7 @@ constexpr uint32_t TM_O = 0;     // 256 fp32 columns: this CTA's value half
 constexpr uint32_t TM_Q = 256;   // 32 QT columns: Q latent dims [0, 64 QT) of the CTA's, 16-bit pairs
 constexpr uint32_t TM_S = TM_Q + 32 * QT;  // NB 64-column score buffers
 static_assert(TM_S + NB * T <= 512, "TMEM columns");
+static_assert((NS & (NS - 1)) == 0, "stage ring indexed by masking");
 constexpr uint32_t TM_COLS = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before a rescale
@@ -302,54 +303,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = ptx::idesc_f16(128, 256, 1u, false, true);
       bool ok = wait(c, ptx::smem_u32(&bars.q_ready), 0);
       ptx::tc_fence_after();
-      const uint32_t qs = sbase + OFF_QS, qr = sbase + OFF_QROPE;
-      auto issue_qk = [&](int u) {
-        const int s = u % NB;
-        const uint32_t d = tmem + TM_S + s * T;
-        const uint32_t st = sbase + OFF_STAGE + (u % NS) * STAGE;
+      // Operand descriptors from bases: the start address is the low field in
+      // 16-byte units, so a stage (STAGE bytes), a slab (ATOM) or a 16-key
+      // step of V (2048) is an add (no carry: every address is below 256 KB).
+      const uint64_t dk = kdesc128(sbase + OFF_STAGE);          // latent slab 0 of stage 0
+      const uint64_t dr = kdesc64(sbase + OFF_STAGE + 4 * ATOM);  // rope slab of stage 0
+      const uint64_t dv = vdesc(sbase + OFF_STAGE);             // V of stage 0
+      const uint64_t dq = kdesc128(sbase + OFF_QS);             // Q's shared-memory slabs
+      const uint64_t dqr = kdesc64(sbase + OFF_QROPE);          // Q's rope half
+      constexpr uint32_t kStageU = STAGE >> 4, kAtomU = ATOM >> 4, kQSlabU = QSLAB >> 4;
+      auto issue_qk = [&](int sb, int sg) {  // into score buffer sb from stage sg
+        const uint32_t d = tmem + TM_S + sb * T;
+        const uint64_t k0 = dk + sg * kStageU, r0 = dr + sg * kStageU;
         for (int a = 0; a < QT; ++a)  // latent dims [0, 64 QT): A from TMEM
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, kdesc128(st + a * ATOM + kk * 32), id_qk,
-                        (a | kk) != 0);
+            ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, k0 + a * kAtomU + 2 * kk, id_qk, (a | kk) != 0);
         for (int a = QT; a < 4; ++a)  // latent dims [64 QT, 256): A from shared memory
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ss(d, kdesc128(qs + (a - QT) * QSLAB + kk * 32), kdesc128(st + a * ATOM + kk * 32),
-                        id_qk, 1);
+            ptx::mma_ss(d, dq + (a - QT) * kQSlabU + 2 * kk, k0 + a * kAtomU + 2 * kk, id_qk, 1);
         for (int kk = 0; kk < 2; ++kk)  // this CTA's 32 rope dims
-          ptx::mma_ss(d, kdesc64(qr + kk * 32), kdesc64(st + 4 * ATOM + kk * 32), id_qk, 1);
-        ptx::mma_commit(ptx::smem_u32(&bars.s_full[s]));
+          ptx::mma_ss(d, dqr + 2 * kk, r0 + 2 * kk, id_qk, 1);
+        ptx::mma_commit(ptx::smem_u32(&bars.s_full[sb]));
       };
-      auto issue_pv = [&](int t, bool second) {
-        const int s = t % NB;
-        const uint32_t pa = tmem + TM_S + s * T;
-        const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
+      auto issue_pv = [&](int t, int sb, int sg, bool second) {
+        const uint32_t pa = tmem + TM_S + sb * T;
+        const uint64_t v0 = dv + sg * kStageU;
         for (int kk = 0; kk < T / 16; ++kk)
-          ptx::mma_ts(tmem + TM_O, pa + kk * 8, vdesc(st + kk * 2048), id_pv, (t | kk) != 0);
+          ptx::mma_ts(tmem + TM_O, pa + kk * 8, v0 + kk * (2048 >> 4), id_pv, (t | kk) != 0);
         if (second)
           for (int kk = 0; kk < T / 16; ++kk)
-            ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, vdesc(st + kk * 2048), id_pv, 1);
-        ptx::mma_commit(ptx::smem_u32(&bars.o_done[s]));
+            ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, v0 + kk * (2048 >> 4), id_pv, 1);
+        ptx::mma_commit(ptx::smem_u32(&bars.o_done[sb]));
         if (t == n_tiles - 1) ptx::mma_commit(ptx::smem_u32(&bars.o_final));
-        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
+        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[sg]));
       };
       // Ready-first issue: QK^T of tile nq once its stage has landed and its
       // score buffer is free (the PV of tile nq - 3 is issued; one thread's
-      // MMAs run in order), PV of tile np once its weights are written.
+      // MMAs run in order), PV of tile np once its weights are written.  The
+      // ring positions and phases are counted, not divided out.
       int nq = 0, np = 0;
+      int bq = 0, bp = 0;            // score buffers of tiles nq and np (t % NB)
+      uint32_t pp = 0;               // phase parity of tile np's weights barrier
       uint64_t t_last = ptx::globaltimer_ns();
       uint32_t idle = 0;
       while (ok && np < n_tiles) {
         bool progress = false;
         if (nq < n_tiles && nq <= np + NB - 1 &&
-            ptx::mbar_test_wait(ptx::smem_u32(&bars.kv_full[nq % NS]), (nq / NS) & 1)) {
+            ptx::mbar_test_wait(ptx::smem_u32(&bars.kv_full[nq & (NS - 1)]), (nq / NS) & 1)) {
           ptx::tc_fence_after();
-          issue_qk(nq++);
+          issue_qk(bq, nq & (NS - 1));
+          ++nq;
+          bq = bq == NB - 1 ? 0 : bq + 1;
           progress = true;
         }
-        if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np % NB]), (np / NB) & 1)) {
+        if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[bp]), pp)) {
           ptx::tc_fence_after();
-          const bool second = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[np % NB]) != 0;
-          issue_pv(np++, second);
+          const bool second = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[bp]) != 0;
+          issue_pv(np, bp, np & (NS - 1), second);
+          ++np;
+          if (bp == NB - 1) {
+            bp = 0;
+            pp ^= 1u;
+          } else {
+            ++bp;
+          }
           progress = true;
         }
         if (progress) {
@@ -358,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           continue;
         }
         if (nq < n_tiles && nq <= np + NB - 1) __nanosleep(32);
-        else (void)ptx::mbar_try_wait(ptx::smem_u32(&bars.p_full[np % NB]), (np / NB) & 1);
+        else (void)ptx::mbar_try_wait(ptx::smem_u32(&bars.p_full[bp]), pp);
         if ((++idle & 15) == 0) {
           const uint64_t now = ptx::globaltimer_ns();
           if (t_last == 0) t_last = now;
@@ -528,15 +545,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Tile t's partial scores -> the partner warp's receive buffer, rounded
     // to 24 bits and packed four to three words, once the partner has read
     // tile t - 1 from it.
-    auto send = [&](int t) -> bool {
-      if (!wait_all(c, ptx::smem_u32(&bars.s_full[t % NB]), (t / NB) & 1)) return false;
+    // (bt3, ph3: tile t's score buffer, t % 3, and that barrier's phase parity.)
+    auto send = [&](int t, int bt3, uint32_t ph3) -> bool {
+      if (!wait_all(c, ptx::smem_u32(&bars.s_full[bt3]), ph3)) return false;
       ptx::tc_fence_after();
       if (t >= 1) {
         if (lane == 0) ptx::mbar_arrive_expect_tx(recv_free, 4);
         if (!wait_all(c, recv_free, (t - 1) & 1)) return false;
       }
       uint32_t raw[32];
-      ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_S + (t % NB) * T, raw);
+      ptx::tmem_ld16x256b_x8(tmem + lanes16 + TM_S + bt3 * T, raw);
       ptx::tmem_ld_wait();
       const uint32_t dst = ptx::mapa(my_recv, peer) + lane * 16;
       const uint32_t bar = ptx::mapa(recv_full, peer);
@@ -556,15 +574,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     bool ok = true;
-    for (int t = 0; ok && t < n_tiles; ++t) {
-      const int bt3 = t % NB;
+    int bt3 = 0;       // t % NB, counted
+    uint32_t ph3 = 0;  // (t / NB) & 1
+    for (int t = 0; ok && t < n_tiles; ++t, ph3 ^= (bt3 == NB - 1), bt3 = bt3 == NB - 1 ? 0 : bt3 + 1) {
       if (!live) {
-        if (!wait_all(c, ptx::smem_u32(&bars.s_full[bt3]), (t / NB) & 1)) { ok = false; break; }
+        if (!wait_all(c, ptx::smem_u32(&bars.s_full[bt3]), ph3)) { ok = false; break; }
         if (lane == 0) reinterpret_cast<volatile uint8_t*>(&bars.heavy[bt3])[sw] = 0;
         ptx::mbar_arrive(ptx::smem_u32(&bars.p_full[bt3]));
         continue;
       }
-      if (!send(t)) { ok = false; break; }
+      if (!send(t, bt3, ph3)) { ok = false; break; }
       // Tile t: the partner's block and this CTA's own exact partial scores
       // (still in score buffer t % 3).
       if (lane == 0) ptx::mbar_arrive_expect_tx(recv_full, RECV_W);
@@ -646,8 +665,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (t > 0) {
           // The PV of tile t - 1 must have finished accumulating: its barrier
           // in the ring is at most one phase short (see the file comment).
-          const int tp = t - 1;
-          if (!wait_all(c, ptx::smem_u32(&bars.o_done[tp % NB]), (tp / NB) & 1)) { ok = false; break; }
+          const int bprev = bt3 == 0 ? NB - 1 : bt3 - 1;  // tile t - 1's ring slot and phase
+          const uint32_t pprev = bt3 == 0 ? ph3 ^ 1u : ph3;
+          if (!wait_all(c, ptx::smem_u32(&bars.o_done[bprev]), pprev)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
