@@ -383,53 +383,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = ptx::idesc_f16(128, 256, kAB, false, true);
       bool ok = wait(c, ptx::smem_u32(&bars.q_ready), 0);
       ptx::tc_fence_after();
-      auto issue_qk = [&](int u) {
-        const int s = u % NS;
+      // Operand descriptors from bases: the start address is the low field in
+      // 16-byte units, so a stage, a slab or a 16-key step of V is an add (no
+      // carry: every address is below 256 KB).
+      const uint64_t dk = kmajor_desc(sbase + OFF_STAGE);  // slab 0 of stage 0
+      const uint64_t dv = vmajor_desc(sbase + OFF_STAGE);  // V of stage 0
+      const uint64_t dqr = kmajor_desc(sbase + OFF_QROPE);
+      constexpr uint32_t kStageU = STAGE >> 4, kAtomU = ATOM >> 4;
+      auto issue_qk = [&](int u, int s) {  // tile u from stage s (u % NS)
         const uint32_t d = tmem + TM_S + (u & 1) * T;
-        const uint32_t st = sbase + OFF_STAGE + s * STAGE;
+        const uint64_t k0 = dk + s * kStageU;
         for (int a = 0; a < 4; ++a)
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, kmajor_desc(st + a * ATOM + kk * 32),
-                        id_qk, (a | kk) != 0);
-        {  // this CTA's 32 rope dims: 16-dim steps 2 rank, 2 rank + 1 of the rope slab
-          const uint32_t qr = sbase + OFF_QROPE;
-          for (int kk = 2 * (int)rank; kk < 2 * (int)rank + 2; ++kk)
-            ptx::mma_ss(d, kmajor_desc(qr + kk * 32), kmajor_desc(st + 4 * ATOM + kk * 32), id_qk, 1);
-        }
+            ptx::mma_ts(d, tmem + TM_Q + a * 32 + kk * 8, k0 + a * kAtomU + 2 * kk, id_qk,
+                        (a | kk) != 0);
+        // this CTA's 32 rope dims: 16-dim steps 2 rank, 2 rank + 1 of the rope slab
+        for (int kk = 2 * (int)rank; kk < 2 * (int)rank + 2; ++kk)
+          ptx::mma_ss(d, dqr + 2 * kk, k0 + 4 * kAtomU + 2 * kk, id_qk, 1);
         ptx::mma_commit(ptx::smem_u32(&bars.s_full[u & 1]));
       };
-      auto issue_pv = [&](int t, bool second) {
+      auto issue_pv = [&](int t, int s, bool second) {  // tile t from stage s (t % NS)
         const uint32_t pa = tmem + TM_S + (t & 1) * T;
-        const uint32_t st = sbase + OFF_STAGE + (t % NS) * STAGE;
+        const uint64_t v0 = dv + s * kStageU;
         for (int kk = 0; kk < T / 16; ++kk)
-          ptx::mma_ts(tmem + TM_O, pa + kk * 8, vmajor_desc(st + kk * 2048), id_pv, (t | kk) != 0);
+          ptx::mma_ts(tmem + TM_O, pa + kk * 8, v0 + kk * (2048 >> 4), id_pv, (t | kk) != 0);
         if (!kFp8 && second) {  // second-order weights (see the softmax)
           for (int kk = 0; kk < T / 16; ++kk)
-            ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, vmajor_desc(st + kk * 2048), id_pv, 1);
+            ptx::mma_ts(tmem + TM_O, pa + 32 + kk * 8, v0 + kk * (2048 >> 4), id_pv, 1);
         }
         ptx::mma_commit(ptx::smem_u32(&bars.o_done));
         if (t == n_tiles - 1) ptx::mma_commit(ptx::smem_u32(&bars.o_final));
-        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[t % NS]));
+        ptx::mma_commit(ptx::smem_u32(&bars.kv_empty[s]));
       };
       // Issue whichever is ready: QK^T of tile nq (its stage has landed and
       // its score buffer is free, i.e. the PV of tile nq-2 is issued; the
       // tensor pipe runs one thread's MMAs in order) or PV of tile np (its
       // weights are written).  A late stage never holds back a ready PV.
+      // The stage ring's positions and phases are counted, not divided out.
       int nq = 0, np = 0;
+      int sq = 0, sp = 0;     // stages of tiles nq and np (t % NS)
+      uint32_t phq = 0;       // phase parity of tile nq's stage barrier
       uint64_t t_last = ptx::globaltimer_ns();
       uint32_t idle = 0;
       while (ok && np < n_tiles) {
         bool progress = false;
         if (nq < n_tiles && nq <= np + 1 &&
-            ptx::mbar_test_wait(ptx::smem_u32(&bars.kv_full[nq % NS]), (nq / NS) & 1)) {
+            ptx::mbar_test_wait(ptx::smem_u32(&bars.kv_full[sq]), phq)) {
           ptx::tc_fence_after();
-          issue_qk(nq++);
+          issue_qk(nq++, sq);
+          if (sq == NS - 1) {
+            sq = 0;
+            phq ^= 1u;
+          } else {
+            ++sq;
+          }
           progress = true;
         }
         if (np < nq && ptx::mbar_test_wait(ptx::smem_u32(&bars.p_full[np & 1]), (np >> 1) & 1)) {
           ptx::tc_fence_after();
           const bool second = *reinterpret_cast<volatile uint64_t*>(&bars.heavy[np & 1]) != 0;
-          issue_pv(np++, second);
+          issue_pv(np++, sp, second);
+          sp = sp == NS - 1 ? 0 : sp + 1;
           progress = true;
         }
         if (progress) {
